@@ -1,0 +1,327 @@
+"""CPU oracle for the MoE expert-parallel layout -> dispatch -> combine path.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline leg may import this package.  It shares no code
+with the CUDA path (``combine_ep_layout_03_gb300``) and never imports it.
+
+The arithmetic lives in ``ep_oracle.c`` (plain C, compiled here with gcc, no
+FMA contraction, no fast-math); this module only marshals numpy arrays.  Each
+wrapped function cites, in the C source, the passage of the pages it follows:
+the DeepEP "Normal Mode API" (dispatch/combine parameters and returns), CANN
+"aclnnMoeDistributeDispatchV2" (Formula section: quantMode 0, 2 and 4) and
+Modular MAX "EPBatchManager" (ep_dispatch outputs, ep_combine).
+
+Parity pins: every function here is pinned by the CPU tests in
+``tests/test_oracle_*.py`` against brute force, closed forms, library
+routines and hand-worked rows.  Two readings are not fixed by any value on the
+pages and are marked "parity unpinned": the e8m0 byte stores the decode scale
+2^sharedExp (not its inverse), and e2m1 packs element 2i in the low nibble.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ep_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libeporacle.so")
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+# quant-mode numbers of the C-ABI enum
+Q_NONE, Q_INT8, Q_E4M3, Q_E5M2, Q_E2M1 = 0, 2, 4, 5, 6
+QUANT_MODES = (Q_NONE, Q_INT8, Q_E4M3, Q_E5M2, Q_E2M1)
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle into a shared library (gcc).  Returns its path."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else ctypes.c_void_p(0)
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) and return the ctypes library."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _declare(ctypes.CDLL(path))
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+        return _lib
+
+
+def _declare(lib):
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
+    lib.oracle_bf16_from_f32.restype = ctypes.c_uint16
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.oracle_mini_encode.argtypes = [i32, ctypes.c_float]
+    lib.oracle_mini_encode.restype = i32
+    lib.oracle_mini_decode.argtypes = [i32, i32]
+    lib.oracle_mini_decode.restype = ctypes.c_double
+    lib.oracle_quant_int8_row.argtypes = [i32, vp, vp, vp]
+    lib.oracle_quant_mx_row.argtypes = [i32, i32, vp, vp, vp]
+    lib.oracle_row_data_bytes.argtypes = [i32, i32]
+    lib.oracle_row_data_bytes.restype = i64
+    lib.oracle_row_scale_bytes.argtypes = [i32, i32]
+    lib.oracle_row_scale_bytes.restype = i64
+    lib.oracle_layout.argtypes = [i32, i32, i32, i32, i32, vp, i64] + [vp] * 12
+    lib.oracle_layout.restype = i32
+    lib.oracle_dispatch.argtypes = [i32, i32, i32, i32, vp, vp, i64, i64, vp, vp]
+    lib.oracle_dispatch_rows.argtypes = [i64, vp, vp, i32, i32, vp, vp, vp]
+    lib.oracle_expert_rows.argtypes = [i64, vp, vp, i32, i32, vp, vp, i32, vp]
+    lib.oracle_combine.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp]
+    lib.oracle_combine_ref64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp, vp]
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# scalar encoders
+# ---------------------------------------------------------------------------
+
+def bf16_from_f32(values) -> np.ndarray:
+    lib = load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_bf16_from_f32(float(x)) for x in v], dtype=np.uint16)
+
+
+def mini_encode(q: int, values) -> np.ndarray:
+    lib = load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_mini_encode(q, float(x)) for x in v], dtype=np.int32)
+
+
+def mini_decode(q: int, codes) -> np.ndarray:
+    lib = load()
+    return np.array([lib.oracle_mini_decode(q, int(c)) for c in np.asarray(codes).ravel()])
+
+
+def row_bytes(q: int, H: int) -> tuple[int, int]:
+    lib = load()
+    return int(lib.oracle_row_data_bytes(q, H)), int(lib.oracle_row_scale_bytes(q, H))
+
+
+# ---------------------------------------------------------------------------
+# quantisation of single rows
+# ---------------------------------------------------------------------------
+
+def quant_int8_row(x_bf16: np.ndarray) -> tuple[np.ndarray, np.float32]:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    q = np.zeros(x.shape[-1], dtype=np.int8)
+    inv = np.zeros(1, dtype=np.float32)
+    load().oracle_quant_int8_row(x.shape[-1], _p(x), _p(q), _p(inv))
+    return q, inv[0]
+
+
+def quant_mx_row(q: int, x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    H = x.shape[-1]
+    db, sb = row_bytes(q, H)
+    codes = np.zeros(db, dtype=np.uint8)
+    scales = np.zeros(sb, dtype=np.uint8)
+    load().oracle_quant_mx_row(H, q, _p(x), _p(codes), _p(scales))
+    return codes, scales
+
+
+# ---------------------------------------------------------------------------
+# layout
+# ---------------------------------------------------------------------------
+
+class Layout:
+    """Result of :func:`layout` (numpy arrays, shapes as in the C source)."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+    @property
+    def rows(self) -> int:
+        return int(self.rank_base[-1])
+
+
+def layout(R: int, T: int, E: int, K: int, alpha: int, topk: np.ndarray,
+           recv_cap: int | None = None) -> Layout:
+    topk = np.ascontiguousarray(topk, dtype=np.int64).reshape(R * T * K)
+    L = E // R
+    if recv_cap is None:
+        recv_cap = R * T * K + E * (alpha - 1)
+    out = dict(
+        cnt=np.zeros((R, E), np.int32),
+        is_token_in_rank=np.zeros((R, T, R), np.uint8),
+        num_tokens_per_rank=np.zeros((R, R), np.int32),
+        recv_cnt=np.zeros(E, np.int32),
+        aligned=np.zeros(E, np.int32),
+        expert_start=np.zeros((R, L + 1), np.int32),
+        rank_base=np.zeros(R + 1, np.int64),
+        src_prefix=np.zeros((R, E), np.int32),
+        dst_row=np.zeros((R, T, K), np.int32),
+        recv_src=np.full(max(recv_cap, 1), -1, np.int32),
+        expert_ids=np.zeros((R, L), np.int32),
+        expert_usage_stats=np.zeros((R, 2), np.int32),
+    )
+    st = load().oracle_layout(
+        R, T, E, K, alpha, _p(topk), recv_cap,
+        *(_p(out[k]) for k in ("cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt",
+                               "aligned", "expert_start", "rank_base", "src_prefix", "dst_row",
+                               "recv_src", "expert_ids", "expert_usage_stats")))
+    rows = int(out["rank_base"][-1])
+    out["recv_src"] = out["recv_src"][: min(rows, recv_cap)]
+    return Layout(status=int(st), R=R, T=T, E=E, K=K, alpha=alpha, L=L, **out)
+
+
+def row_expert(lay: Layout) -> np.ndarray:
+    """Expert id of every receive row (padding rows included)."""
+    e = np.repeat(np.arange(lay.E, dtype=np.int32), lay.aligned.astype(np.int64))
+    return e.astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# dispatch
+# ---------------------------------------------------------------------------
+
+def dispatch(lay: Layout, x_bf16: np.ndarray, q: int, row_begin: int = 0,
+             row_end: int | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Receive rows [row_begin, row_end) as (data bytes [rows, db], scale bytes [rows, sb])."""
+    N = lay.R * lay.T
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    H = x.shape[1]
+    if row_end is None:
+        row_end = lay.rows
+    db, sb = row_bytes(q, H)
+    n = row_end - row_begin
+    data = np.zeros((n, db), np.uint8)
+    scales = np.zeros((n, sb), np.uint8)
+    dr = np.ascontiguousarray(lay.dst_row.reshape(-1))
+    load().oracle_dispatch(N, lay.K, H, q, _p(dr), _p(x), row_begin, row_end, _p(data),
+                           _p(scales) if sb else None)
+    return data, scales
+
+
+def dispatch_rows(lay: Layout, x_bf16: np.ndarray, q: int, rows: np.ndarray):
+    """Selected receive rows, computed one by one through recv_src."""
+    N = lay.R * lay.T
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    H = x.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    db, sb = row_bytes(q, H)
+    data = np.zeros((len(rows), db), np.uint8)
+    scales = np.zeros((len(rows), sb), np.uint8)
+    rs = np.ascontiguousarray(lay.recv_src)
+    load().oracle_dispatch_rows(len(rows), _p(rows), _p(rs), H, q, _p(x), _p(data),
+                                _p(scales) if sb else None)
+    return data, scales
+
+
+def expert_rows(lay: Layout, rows: np.ndarray, H: int, q: int, data: np.ndarray,
+                scales: np.ndarray, mark_mod: int = 0) -> np.ndarray:
+    """Stand-in expert output (bf16 bits) for receive rows given their bytes."""
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    re = np.ascontiguousarray(row_expert(lay))
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    y = np.zeros((len(rows), H), np.uint16)
+    load().oracle_expert_rows(len(rows), _p(rows), _p(re), H, q, _p(data),
+                              _p(scales) if scales.size else None, mark_mod, _p(y))
+    return y
+
+
+# ---------------------------------------------------------------------------
+# combine
+# ---------------------------------------------------------------------------
+
+def combine(lay: Layout, y_bf16: np.ndarray, w: np.ndarray, shared: np.ndarray | None = None,
+            tok_begin: int = 0, tok_end: int | None = None,
+            y_rows: np.ndarray | None = None) -> np.ndarray:
+    """bf16 bits of out[tok_begin:tok_end]; y_rows maps receive row -> row of y."""
+    R, T, K = lay.R, lay.T, lay.K
+    if tok_end is None:
+        tok_end = R * T
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    H = y.shape[-1]
+    S = 0 if shared is None else shared.shape[1]
+    sh = None if shared is None else np.ascontiguousarray(shared, dtype=np.uint16)
+    wf = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    dr = np.ascontiguousarray(lay.dst_row.reshape(-1))
+    yr = None if y_rows is None else np.ascontiguousarray(y_rows, dtype=np.int64)
+    out = np.zeros((tok_end - tok_begin, H), np.uint16)
+    load().oracle_combine(R, T, H, K, S, _p(dr), _p(wf), _p(y), _p(yr), _p(sh),
+                          tok_begin, tok_end, _p(out))
+    return out
+
+
+def combine_ref64(lay: Layout, y_bf16: np.ndarray, w: np.ndarray,
+                  shared: np.ndarray | None = None, tok_begin: int = 0,
+                  tok_end: int | None = None, y_rows: np.ndarray | None = None):
+    """(fp64 sum, fp64 sum of |terms|) for out[tok_begin:tok_end]."""
+    R, T, K = lay.R, lay.T, lay.K
+    if tok_end is None:
+        tok_end = R * T
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    H = y.shape[-1]
+    S = 0 if shared is None else shared.shape[1]
+    sh = None if shared is None else np.ascontiguousarray(shared, dtype=np.uint16)
+    wf = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    dr = np.ascontiguousarray(lay.dst_row.reshape(-1))
+    yr = None if y_rows is None else np.ascontiguousarray(y_rows, dtype=np.int64)
+    ref = np.zeros((tok_end - tok_begin, H), np.float64)
+    mag = np.zeros((tok_end - tok_begin, H), np.float64)
+    load().oracle_combine_ref64(R, T, H, K, S, _p(dr), _p(wf), _p(y), _p(yr), _p(sh),
+                                tok_begin, tok_end, _p(ref), _p(mag))
+    return ref, mag
+
+
+# ---------------------------------------------------------------------------
+# tolerance
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (normal range: 2^(floor(log2|v|) - 7))."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, e = np.frexp(a)  # a = m * 2^e, m in [0.5, 1)
+    ulp = np.ldexp(1.0, e - 8)
+    return np.maximum(ulp, np.ldexp(1.0, -133))
+
+
+def combine_tolerance_floor(mag: np.ndarray, K: int, S: int) -> np.ndarray:
+    """Error floor of a binary32 sum of K weighted terms plus S shared terms:
+    each multiply and add rounds once (<= 2^-24 relative), so the accumulated
+    error is at most (2K + S + 1) * 2^-24 * sum|terms|."""
+    return np.ldexp(mag, -24) * (2 * K + S + 1)
+
+
+def combine_within_tolerance(got_bits: np.ndarray, ref: np.ndarray, mag: np.ndarray,
+                             K: int, S: int = 0):
+    """Combine tolerance, derived from the arithmetic (fp32 accumulation, one bf16
+    rounding at the end):
+      every element: |got - ref| <= 2 ulp_bf16(ref) + (2K+S+1) 2^-24 sum|terms|;
+      elements with |ref| >= 2^-10 sum|terms| (no heavy cancellation):
+      max |got - ref| / |ref| <= 1e-2.
+    ref is the float64 sum.  Returns (ok, max_abs_excess, max_rel)."""
+    got = bf16_bits_to_f64(got_bits)
+    err = np.abs(got - ref)
+    bound = 2.0 * ulp_bf16(ref) + combine_tolerance_floor(mag, K, S)
+    excess = float(np.max(err - bound)) if err.size else 0.0
+    sel = np.abs(ref) >= np.ldexp(mag, -10)
+    rel = float(np.max(err[sel] / np.abs(ref[sel]))) if np.any(sel) else 0.0
+    return bool(excess <= 0.0 and rel <= 1e-2), excess, rel

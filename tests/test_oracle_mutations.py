@@ -1,0 +1,101 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each case copies the oracle's C source, plants one mistake (a dropped term, a
+wrong or transposed index, a wrong constant, a wrong rounding rule), builds the
+copy with gcc into a temporary directory and runs the pin checks against it:
+at least one pin must fail.  The committed oracle is never modified.
+"""
+import contextlib
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_dispatch_combine as tdc
+import test_oracle_layout as tl
+import test_oracle_quant as tq
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ep_oracle.c")
+
+MUTANTS = {
+    "layout_drop_running_position": ("pos[e] += 1;", ""),
+    "layout_inclusive_source_prefix": (
+        "src_prefix[(int64_t)s * E + e] = acc;\n            acc += cnt[(int64_t)s * E + e];",
+        "acc += cnt[(int64_t)s * E + e];\n            src_prefix[(int64_t)s * E + e] = acc;"),
+    "layout_alignment_off_by_one": ("aligned[e] = ((c + alpha - 1) / alpha) * alpha;",
+                                    "aligned[e] = ((c + alpha) / alpha) * alpha;"),
+    "layout_rank_of_expert_modulo": ("itr[n * R + e / L] = 1;", "itr[n * R + e % R] = 1;"),
+    "layout_transposed_expert_map": ("int j = (int)(e / L), l = (int)(e % L);",
+                                     "int j = (int)(e % R), l = (int)(e / R);"),
+    "int8_wrong_type_max": ("float s = 127.0f / amax;", "float s = 128.0f / amax;"),
+    "int8_inverse_as_amax_over_127": ("*inv = 1.0f / s;", "*inv = amax / 127.0f;"),
+    "int8_round_half_up": ("return (fmodf(f, 2.0f) == 0.0f) ? f : f + 1.0f;", "return f + 1.0f;"),
+    "mx_exponent_off_by_one": ("se = (expfield - 127) - m.emax;", "se = (expfield - 127) - m.emax + 1;"),
+    "mx_e2m1_nibble_swap": ("codes[h / 2] |= (uint8_t)(c << (4 * (h & 1)));",
+                            "codes[h / 2] |= (uint8_t)(c << (4 * (1 - (h & 1))));"),
+    "minifloat_ties_away": ("if (dhi < dlo || (dhi == dlo && (c & 1))) c = c + 1;",
+                            "if (dhi <= dlo) c = c + 1;"),
+    "minifloat_subnormal_scale": ("if (ef == 0) return ldexp((double)mf, 1 - m.bias - m.mbits);",
+                                  "if (ef == 0) return ldexp((double)mf, -m.bias - m.mbits);"),
+    "bf16_ties_up": ("else pick = (lo & 1u) ? hi : lo;", "else pick = hi;"),
+    "combine_first_weight_only": ("float prod = w[n * K + k] * oracle_bf16_to_f32(y[yr * H + h]);",
+                                  "float prod = w[n * K] * oracle_bf16_to_f32(y[yr * H + h]);"),
+    "combine_shared_axes_transposed": (
+        "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
+        "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
+}
+
+
+def pins():
+    """Cheap subset of the pin tests, each a zero-argument callable."""
+    cases = [lambda: tl.test_exhaustive_tiny(),
+             lambda: tl.test_workload1_matches_brute_force(),
+             lambda: tl.test_edge_cases()]
+    cases += [lambda s=s: tl.test_random_small(s) for s in range(8)]
+    cases += [lambda c=c: tq.test_int8_golden(c) for c in tq.read_cases("int8_rows.txt")]
+    cases += [lambda c=c: tq.test_mx_golden(c) for c in tq.read_cases("mx_blocks.txt")]
+    cases += [tq.test_e2m1_nibble_order, tq.test_bf16_matches_torch_cast,
+              tq.test_e2m1_encode_matches_rounding_route]
+    import torch
+    cases += [lambda: tq.test_fp8_decode_table_matches_torch("e4m3", torch.float8_e4m3fn, 0x7e),
+              lambda: tq.test_fp8_encode_matches_torch_in_range("e4m3", torch.float8_e4m3fn, 0x7e)]
+    cases += [lambda: tdc.test_combine_identity_and_marked_experts(1, 64, 4),
+              lambda: tdc.test_combine_identity_and_marked_experts(5, 8, 0)]
+    return cases
+
+
+@contextlib.contextmanager
+def use_library(path):
+    saved = oracle._lib
+    oracle._lib = oracle.load(path)
+    try:
+        yield
+    finally:
+        oracle._lib = saved
+
+
+def test_unmutated_oracle_passes_the_pin_subset():
+    for check in pins():
+        check()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {name}"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", so, str(mutant_c), "-lm"], check=True)
+    caught = 0
+    with use_library(so):
+        for check in pins():
+            try:
+                check()
+            except AssertionError:
+                caught += 1
+                break
+    assert caught, f"no pin caught the planted mistake {name}"
