@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark: one step = the whole hot path over one batch of seeded synthetic
+routing -- layout (3 kernels) -> dispatch -> combine -- on one GPU holding all
+R logical expert-parallel ranks.
+
+Default workload: R=8 ranks x 4096 tokens, H=7168 bf16, 256 experts, top-8
+distinct uniform, softmax weights, alpha=1, no quantisation, identity experts
+(the combine reads the receive buffer).  ``--workload`` picks another one
+(1, 2, 3, 4a, 4b, 5) for local measurement; the default line is workload 2.
+
+Prints one JSON line.  ``value`` is source tokens per second with inputs
+resident in HBM (inputs are larger than L2, so no flush is needed); ``e2e`` is
+the same metric through the library's public calls with pinned host buffers,
+host->device copies of x / topk / weights and the device->host copy of the
+combined output inside the timed region.  ``--impl reference`` times the CPU
+oracle (the only other implementation of this path) on a bounded sample.
+
+Multi-GPU (torchrun): replicas -- every rank runs the full workload on its own
+GPU, no data-path collective; value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s vs GB300 peak, 1 GPU"
+WORKLOAD_KEYS = {"1": (1, 0), "2": (2, 0), "3": (3, 2), "4a": (4, 4), "4b": (4, 6), "5": (5, 0)}
+QNAME = {0: "none", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2", 6: "mxfp4_e2m1"}
+KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "layout": "layout.cu"}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="2", choices=sorted(WORKLOAD_KEYS))
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(name: str) -> str:
+    p = os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (p, os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", "ep_internal.cuh")):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest(KERNEL_SOURCES[kernel])
+    pat = re.compile(r"^\|\s*%s\s*\|\s*%s\s*\|\s*([0-9]+)\s*\|\s*([0-9a-f]+)\s*\|" % (kernel, workload))
+    with open(path) as f:
+        for line in f:
+            m = pat.match(line.strip())
+            if m and m.group(2) == digest:
+                return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float, w0: float):
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not win:
+            win = [p for (t, p) in self.samples if w0 <= t <= t1 + 0.2]
+            window = "warmup+timed"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none"}
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower() == "active"})
+        pw = [num(p[2]) for p in win if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(win), "window": window}
+
+
+def nvsmi_index(dev: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [s for s in vis.split(",") if s.strip()]
+    if ids and all(s.strip().isdigit() for s in ids) and dev < len(ids):
+        return int(ids[dev])
+    return dev
+
+
+# --------------------------------------------------------------------- workload
+
+def make_inputs(w, device):
+    from combine_ep_layout_03_gb300 import synth
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    x_dev = synth.gen_x_device(w, device)
+    sh_dev = synth.gen_shared_device(w, device)
+    return topk, wts, x_dev, sh_dev
+
+
+def algorithmic_bytes(w, quant, rows, V):
+    from combine_ep_layout_03_gb300 import ep
+    db, sb = ep.ep_recv_row_bytes(w.H, quant)
+    N, H, K, S = w.N, w.H, w.K, w.num_shared
+    disp = N * H * 2 + N * K * 4 + rows * (db + sb)
+    comb = V * H * 2 + N * K * 8 + S * N * H * 2 + N * H * 2
+    lay = N * K * 8 * 3 + N * K * 4 + rows * 4 + N * w.R
+    return {"layout": lay, "dispatch": disp, "combine": comb}
+
+
+def run_ours(args, w, quant, rank, local_rank, world):
+    from combine_ep_layout_03_gb300 import ep
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    topk, wts, x_dev, sh_dev = make_inputs(w, dev)
+    topk_dev = torch.from_numpy(topk).to(dev)
+    w_dev = torch.from_numpy(wts).to(dev)
+    lay = ep.EPLayout(w.R, w.T, w.H, w.E, w.K, w.alpha, device=dev)
+    lay.layout(topk_dev)
+    rank_base = lay.recv_rows()
+    rows = int(rank_base[-1])
+    V = int((topk >= 0).sum())
+    data, scales = lay.alloc_recv(quant, max(rows, 1), device=dev)
+    if quant == 0:
+        y = data.view(torch.bfloat16).view(-1, w.H)
+    else:
+        lay.dispatch(x_dev, quant, data, scales)
+        y = torch.empty((max(rows, 1), w.H), dtype=torch.bfloat16, device=dev)
+        lay.expert_identity(quant, data, scales, y)
+    out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        lay.layout(topk_dev)
+        if ev is not None:
+            ev[1].record(stream)
+        lay.dispatch(x_dev, quant, data, scales)
+        if ev is not None:
+            ev[2].record(stream)
+        lay.combine(y, w_dev, out, sh_dev)
+        if ev is not None:
+            ev[3].record(stream)
+
+    sampler = ClockSampler(nvsmi_index(local_rank))
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    t_warm0 = time.time()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert lay.status() == ep.EP_OK
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_timed0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    barrier()
+    torch.cuda.synchronize()
+    t_timed1 = time.time()
+    sampler.stop()
+    total_ms = start.elapsed_time(end)
+    phase = {"layout": [], "dispatch": [], "combine": []}
+    for e in evs:
+        phase["layout"].append(e[0].elapsed_time(e[1]))
+        phase["dispatch"].append(e[1].elapsed_time(e[2]))
+        phase["combine"].append(e[2].elapsed_time(e[3]))
+    assert lay.status() == ep.EP_OK
+
+    # end to end: host buffers, copies in the timed region
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.empty(x_dev.shape, dtype=x_dev.dtype, pin_memory=True)
+        x_host.copy_(x_dev)
+        topk_host = torch.from_numpy(topk).pin_memory()
+        w_host = torch.from_numpy(wts).pin_memory()
+        sh_host = None
+        if sh_dev is not None:
+            sh_host = torch.empty(sh_dev.shape, dtype=sh_dev.dtype, pin_memory=True)
+            sh_host.copy_(sh_dev)
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = x_host.numel() * 2 + topk_host.numel() * 8 + w_host.numel() * 4
+        h2d += 0 if sh_host is None else sh_host.numel() * 2
+        d2h = out_host.numel() * 2
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            topk_dev.copy_(topk_host, non_blocking=True)
+            w_dev.copy_(w_host, non_blocking=True)
+            if sh_host is not None:
+                sh_dev.copy_(sh_host, non_blocking=True)
+            lay.layout(topk_dev)
+            lay.dispatch(x_dev, quant, data, scales)
+            lay.combine(y, w_dev, out, sh_dev)
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(max(2, min(args.warmup, 5))):
+            e2e_step()
+        k2 = max(3, min(args.steps, 50))
+        s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        s2.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        t2.record(stream)
+        barrier()
+        torch.cuda.synchronize()
+        e2e_ms = s2.elapsed_time(t2) / k2
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h, "steps": k2}
+        assert lay.status() == ep.EP_OK
+
+    clocks = sampler.summary(t_timed0, t_timed1, t_warm0)
+    bytes_ = algorithmic_bytes(w, quant, rows, V)
+    return dict(total_ms=total_ms, phase=phase, e2e=e2e, clocks=clocks, bytes=bytes_, rows=rows,
+                V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_dev, sh_dev=sh_dev)
+
+
+# --------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, quant, topk, wts, x_bits, sh0_bits, budget_s):
+    """The oracle as it stands, single-threaded: layout over the whole routing,
+    then dispatch (rows one by one through recv_src) and combine of the first n
+    source tokens of rank 0, n chosen so the work takes about budget_s.
+    Returns (tokens/s, description, seconds spent)."""
+    import oracle
+    t0 = time.perf_counter()
+    olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    t_layout = time.perf_counter() - t0
+    K = w.K
+
+    def run(n):
+        tokens = np.arange(n)
+        d = olay.dst_row.reshape(-1, K)[tokens].reshape(-1)
+        rows = np.unique(d[d >= 0])
+        ymap = np.full(max(olay.rows, 1), -1, np.int64)
+        ymap[rows] = np.arange(len(rows))
+        a = time.perf_counter()
+        data, scales = oracle.dispatch_rows(olay, x_bits, quant, rows)
+        b = time.perf_counter()
+        if quant == 0:
+            y = data.view(np.uint16).reshape(len(rows), w.H)
+        else:
+            y = oracle.expert_rows(olay, rows, w.H, quant, data, scales)
+        c = time.perf_counter()
+        sh = None if sh0_bits is None else sh0_bits
+        oracle.combine(olay, y, wts, sh, 0, n, ymap)
+        dd = time.perf_counter()
+        return (b - a) + (dd - c)
+
+    n = min(w.T, 8)
+    t = run(n)
+    spent = t_layout + t
+    while t < budget_s * 0.5 and n < w.T:
+        n = int(min(w.T, max(n * 2, n * budget_s / max(t, 1e-3))))
+        t = run(n)
+        spent += t
+    per_token = t_layout / w.N + t / n
+    desc = (f"layout of all {w.N} tokens ({t_layout*1e3:.1f} ms) + dispatch and combine of the "
+            f"first {n} tokens of rank 0 ({t:.2f} s), extrapolated per token")
+    return 1.0 / per_token, desc, spent, n
+
+
+def host_x_bits(x_dev, w):
+    return x_dev.contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.N, w.H)
+
+
+def host_shared0(sh_dev, w):
+    if sh_dev is None:
+        return None
+    return sh_dev[0:1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------- main
+
+def workload_config(w, quant, key):
+    from combine_ep_layout_03_gb300 import synth
+    return {"workload": f"ep_layout_dispatch_combine[{key}] " + w.name,
+            "R": w.R, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "alpha": w.alpha,
+            "routing": w.routing, "drop_p": w.drop_p, "num_shared": w.num_shared,
+            "quant": QNAME[quant], "tokens_per_step": w.N,
+            "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas",
+            "experts": "identity (combine reads the receive buffer)" if quant == 0 else
+            "identity after dequantisation, built once before timing"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, local_rank, world = dist_env()
+    from combine_ep_layout_03_gb300 import synth
+    idx, quant = WORKLOAD_KEYS[args.workload]
+    w = synth.WORKLOADS[idx]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, w, quant)
+
+    if world > 1:
+        import datetime
+        torch.distributed.init_process_group("gloo", timeout=datetime.timedelta(minutes=10))
+    res = run_ours(args, w, quant, rank, local_rank, world)
+    K = args.steps
+    ms = res["total_ms"] / K
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([res["total_ms"], res["e2e"]["ms"] if res["e2e"] else 0.0], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        res["total_ms"], e2e_ms = float(t[0]), float(t[1])
+        if res["e2e"]:
+            res["e2e"]["ms"] = e2e_ms
+        ms = res["total_ms"] / K
+    value = world * w.N / (ms / 1e3)
+
+    peak, peak_src = measured_peaks()
+    avg = {k: statistics.fmean(v) for k, v in res["phase"].items()}
+    med = {k: statistics.median(v) for k, v in res["phase"].items()}
+    gbs = {k: res["bytes"][k] / (avg[k] / 1e3) / 1e9 for k in avg}
+    dom = "dispatch" if avg["dispatch"] >= avg["combine"] else "combine"
+    traffic = profiled_traffic(dom, args.workload)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(gbs[dom], 1), "peak": peak,
+                "unit": "GB/s", "frac": round(gbs[dom] / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "algorithmic_bytes": res["bytes"][dom]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xb = host_x_bits(res["x_dev"], w)
+        sh0 = host_shared0(res["sh_dev"], w)
+        v, desc, spent, n = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget)
+        cpu = {"value": round(v, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": desc}
+
+    e2e = None
+    if res["e2e"]:
+        e2e = {"value": round(world * w.N / (res["e2e"]["ms"] / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"],
+               "ms_per_step": round(res["e2e"]["ms"], 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if quant == 0 else f"bf16->{QNAME[quant]}",
+        "data": "synthetic (seeded: x ~ N(0,1) rounded to bf16, routing and softmax weights per "
+                "the workload's recipe; identity experts)",
+        "config": workload_config(w, quant, args.workload),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 5 * K,
+        "clocks": res["clocks"],
+        "kernels": {
+            k: {"avg_ms": round(avg[k], 5), "median_ms": round(med[k], 5),
+                "algorithmic_bytes": res["bytes"][k], "gbs": round(gbs[k], 1),
+                "frac_of_peak": round(gbs[k] / peak, 4)} for k in avg},
+        "rows": res["rows"], "valid_entries": res["V"],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference(args, w, quant):
+    """The CPU oracle as the reference arm: each step times the oracle on a
+    bounded sample of the same workload, on the host cores."""
+    from combine_ep_layout_03_gb300 import synth
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    x_bits = synth.gen_x(w).reshape(w.N, w.H)
+    sh = synth.gen_shared(w.with_(R=1)) if w.num_shared else None
+    budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    vals, descs = [], None
+    for i in range(args.warmup + args.steps):
+        v, desc, spent, n = oracle_sample(w, quant, topk, wts, x_bits, sh, budget)
+        if i >= args.warmup:
+            vals.append(v)
+            descs = desc
+    value = statistics.fmean(vals)
+    ms = w.N / value * 1e3
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if quant == 0 else f"bf16->{QNAME[quant]}",
+        "data": "synthetic (same seeded recipe as the GPU arm)", "impl": "reference",
+        "config": workload_config(w, quant, args.workload),
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle", "sample": descs},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

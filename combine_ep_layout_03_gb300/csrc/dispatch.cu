@@ -1,0 +1,248 @@
+// dispatch.cu -- permute-scatter of token rows into the receive layout, with
+// the encodings of CANN aclnnMoeDistributeDispatchV2's Formula section:
+//   quantMode 0  bf16 copy;
+//   quantMode 2  per-token dynamic int8: s = 127 / max|x|, code = rn(x * s),
+//                scale word 1/s;
+//   quantMode 4  MX: per 32-element block sharedExp = floor(log2(max|x|)) - emax,
+//                code = cast(x / 2^sharedExp) (e4m3 / e5m2, and e2m1 packed x2),
+//                e8m0 scale byte sharedExp + 127.
+//
+// One CTA handles one token at a time (grid-stride, persistent grid).  Each
+// thread holds VPT 16-byte vectors of the row in registers at vector index
+// u * NT + tid, so every warp access is one contiguous 512-byte run.  The row
+// is read once, encoded once, then written to its K destination rows.  Work
+// items past the last token zero the alpha-padding rows, one expert each.
+// The four lanes 4m..4m+3 hold one 32-element MX block at the same u.
+#include "ep_internal.cuh"
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+enum { M_NONE = 0, M_INT8 = 2, M_E4M3 = 4, M_E5M2 = 5, M_E2M1 = 6 };
+
+// |bf16| of the 8 elements of a vector, as the max of the magnitude bits
+// (monotone in the value for finite inputs).
+__device__ __forceinline__ uint32_t vec_absmax_bits(const uint4& v) {
+    const uint32_t m = 0x7fff7fffu;
+    uint32_t a = __vmaxu2(v.x & m, v.y & m);
+    uint32_t b = __vmaxu2(v.z & m, v.w & m);
+    a = __vmaxu2(a, b);
+    return max(a & 0xffffu, a >> 16);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
+    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+    f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xffff0000u);
+    f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xffff0000u);
+}
+
+// int8 code of one element: round half even of fl(x * s), clamped.
+__device__ __forceinline__ uint32_t q8(float x, float s) {
+    int q = __float2int_rn(__fmul_rn(x, s));
+    q = max(-127, min(127, q));
+    return (uint32_t)q & 0xffu;
+}
+
+template <int Q>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    uint16_t r;
+    if (Q == M_E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 8 floats -> 4 bytes of packed e2m1 (element 2i in the low nibble of byte i).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float f[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(r)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+    return r;
+}
+
+template <int Q>
+struct MxTraits { static constexpr int emax = 0; };
+template <> struct MxTraits<M_E4M3> { static constexpr int emax = 8; };
+template <> struct MxTraits<M_E5M2> { static constexpr int emax = 15; };
+template <> struct MxTraits<M_E2M1> { static constexpr int emax = 2; };
+
+// Zero one padding row region [r0, r1) of data and scales with the whole CTA.
+__device__ void zero_rows(const DispatchArgs& a, int64_t r0, int64_t r1) {
+    if (r1 <= r0) return;
+    const int64_t nbytes = (r1 - r0) * a.row_bytes;
+    uint8_t* base = a.data + r0 * a.row_bytes;
+    if ((a.row_bytes & 15) == 0) {
+        for (int64_t i = threadIdx.x; i < nbytes / 16; i += blockDim.x)
+            st_v4(base + i * 16, make_uint4(0, 0, 0, 0));
+    } else {
+        for (int64_t i = threadIdx.x; i < nbytes / 8; i += blockDim.x)
+            st_v2(base + i * 8, make_uint2(0, 0));
+    }
+    if (a.scale_bytes) {
+        const int64_t sbytes = (r1 - r0) * a.scale_bytes;
+        uint8_t* sb = a.scales + r0 * a.scale_bytes;
+        for (int64_t i = threadIdx.x; i < sbytes; i += blockDim.x) sb[i] = 0;
+    }
+}
+
+template <int Q, int VPT>
+__global__ void __launch_bounds__(256)
+dispatch_kernel(DispatchArgs a) {
+    __shared__ int sdst[kMaxTopk];
+    __shared__ uint32_t sred[8];
+    const int total = a.expert_base[a.E];
+    if ((int64_t)total > a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
+        return;
+    }
+    const int NT = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t items = a.N + a.E;
+    for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
+        if (w >= a.N) {
+            const int e = (int)(w - a.N);
+            const int64_t r0 = (int64_t)a.expert_base[e] + a.recv_cnt[e];
+            const int64_t r1 = a.expert_base[e + 1];
+            zero_rows(a, r0, r1);
+            continue;
+        }
+        __syncthreads();  // sdst / sred of the previous token are consumed
+        if (tid < a.K) sdst[tid] = a.dst_row[w * a.K + tid];
+        const uint16_t* xrow = a.x + w * a.H;
+        uint4 v[VPT];
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * NT + tid;
+            v[u] = vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0);
+        }
+        if constexpr (Q == M_INT8) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) m = max(m, vec_absmax_bits(v[u]));
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+            if (lane == 0) sred[warp] = m;
+        }
+        __syncthreads();
+
+        if constexpr (Q == M_NONE) {
+            for (int k = 0; k < a.K; ++k) {
+                const int d = sdst[k];
+                if (d < 0) continue;
+                uint8_t* row = a.data + (int64_t)d * a.row_bytes;
+#pragma unroll
+                for (int u = 0; u < VPT; ++u) {
+                    const int vi = u * NT + tid;
+                    if (vi < a.nvec) st_v4(row + (int64_t)vi * 16, v[u]);
+                }
+            }
+        } else if constexpr (Q == M_INT8) {
+            uint32_t m = 0;
+            for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i]);
+            const float amax = bf16_bits_to_float(m);
+            const float s = __fdiv_rn(127.0f, amax);      // +inf for an all-zero row
+            const float inv = __fdiv_rn(1.0f, s);          // 0 for an all-zero row
+            uint2 code[VPT];
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                float f[8];
+                unpack8(v[u], f);
+                if (amax > 0.0f) {
+                    code[u].x = q8(f[0], s) | (q8(f[1], s) << 8) | (q8(f[2], s) << 16) | (q8(f[3], s) << 24);
+                    code[u].y = q8(f[4], s) | (q8(f[5], s) << 8) | (q8(f[6], s) << 16) | (q8(f[7], s) << 24);
+                } else {
+                    code[u] = make_uint2(0, 0);
+                }
+            }
+            for (int k = 0; k < a.K; ++k) {
+                const int d = sdst[k];
+                if (d < 0) continue;
+                uint8_t* row = a.data + (int64_t)d * a.row_bytes;
+#pragma unroll
+                for (int u = 0; u < VPT; ++u) {
+                    const int vi = u * NT + tid;
+                    if (vi < a.nvec) st_v2(row + (int64_t)vi * 8, code[u]);
+                }
+                if (tid == 0) reinterpret_cast<float*>(a.scales)[d] = inv;
+            }
+        } else {
+            // MX: block b = vi / 4 lives in lanes 4m..4m+3 at the same u
+            constexpr int emax = MxTraits<Q>::emax;
+            uint32_t packed[VPT][2];
+            uint32_t sbyte[VPT];
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                uint32_t m = vec_absmax_bits(v[u]);
+                m = max(m, __shfl_xor_sync(kFull, m, 1));
+                m = max(m, __shfl_xor_sync(kFull, m, 2));
+                const int ef = (int)(m >> 7) & 0xff;                 // bf16 exponent field
+                int se = (ef == 0) ? -127 : max(ef - 127 - emax, -127);
+                se = min(se, 127);
+                sbyte[u] = (uint32_t)(se + 127);
+                const float mul = __uint_as_float((uint32_t)(127 - se) << 23);  // 2^-se, exact
+                float f[8];
+                unpack8(v[u], f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], mul);
+                if constexpr (Q == M_E2M1) {
+                    packed[u][0] = cvt_e2m1x8(f);
+                    packed[u][1] = 0;
+                } else {
+                    packed[u][0] = cvt_fp8x2<Q>(f[0], f[1]) | (cvt_fp8x2<Q>(f[2], f[3]) << 16);
+                    packed[u][1] = cvt_fp8x2<Q>(f[4], f[5]) | (cvt_fp8x2<Q>(f[6], f[7]) << 16);
+                }
+            }
+            for (int k = 0; k < a.K; ++k) {
+                const int d = sdst[k];
+                if (d < 0) continue;
+                uint8_t* row = a.data + (int64_t)d * a.row_bytes;
+                uint8_t* srow = a.scales + (int64_t)d * a.scale_bytes;
+#pragma unroll
+                for (int u = 0; u < VPT; ++u) {
+                    const int vi = u * NT + tid;
+                    if (vi < a.nvec) {
+                        if constexpr (Q == M_E2M1) st_u32(row + (int64_t)vi * 4, packed[u][0]);
+                        else st_v2(row + (int64_t)vi * 8, make_uint2(packed[u][0], packed[u][1]));
+                        if ((vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int Q>
+cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
+    constexpr int VPT = 4;
+    const int nt = ((a.nvec + VPT - 1) / VPT + 31) / 32 * 32;
+    int occ = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dispatch_kernel<Q, VPT>, nt, 0);
+    if (err != cudaSuccess) return err;
+    const int64_t items = a.N + a.E;
+    int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
+    if (grid > items) grid = items;
+    if (grid < 1) grid = 1;
+    dispatch_kernel<Q, VPT><<<(unsigned)grid, nt, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
+    switch (quant) {
+        case M_NONE: return launch_q<M_NONE>(h, a, st);
+        case M_INT8: return launch_q<M_INT8>(h, a, st);
+        case M_E4M3: return launch_q<M_E4M3>(h, a, st);
+        case M_E5M2: return launch_q<M_E5M2>(h, a, st);
+        case M_E2M1: return launch_q<M_E2M1>(h, a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}

@@ -1,0 +1,327 @@
+// ep_api.cu -- host side of the C ABI declared in include/ep_layout.h:
+// argument validation, workspace carving, handle bookkeeping and launches.
+// The aclnn two-phase convention (CANN aclnnMoeDistributeDispatchV2: query the
+// workspace size, then execute; every call returns a status) shapes the API.
+#include <stdlib.h>
+#include <string.h>
+
+#include "ep_internal.cuh"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool is_mx(int q) { return q == EP_QUANT_MXFP8_E4M3 || q == EP_QUANT_MXFP8_E5M2 || q == EP_QUANT_MXFP4_E2M1; }
+
+bool valid_quant(int q) {
+    return q == EP_QUANT_NONE || q == EP_QUANT_INT8_PER_TOKEN || is_mx(q);
+}
+
+struct Tiling { int32_t C, TPB, B; };
+
+Tiling tiling_of(const ep_params* p) {
+    Tiling t;
+    const int R = p->num_ranks, T = p->tokens_per_rank;
+    if (T == 0) { t.C = 1; t.TPB = 0; t.B = R; return t; }
+    int C = (kLayoutTargetBlocks + R - 1) / R;
+    const int max_c = (T + 31) / 32;  // at least 32 tokens per CTA
+    if (C > max_c) C = max_c;
+    if (C < 1) C = 1;
+    t.TPB = (T + C - 1) / C;
+    t.C = (T + t.TPB - 1) / t.TPB;
+    t.B = R * t.C;
+    return t;
+}
+
+int64_t worst_rows(const ep_params* p) {
+    return (int64_t)p->num_ranks * p->tokens_per_rank * p->topk +
+           (int64_t)p->num_experts * (p->expert_alignment - 1);
+}
+
+int64_t recv_cap_of(const ep_params* p) {
+    return p->recv_capacity_rows > 0 ? p->recv_capacity_rows : worst_rows(p);
+}
+
+// Byte offsets of every workspace array, in one place.
+struct Carve {
+    size_t status, blk_hist, blk_rank, cnt, itr, ntpr, recv_cnt, aligned, expert_start,
+        rank_base, expert_base, src_prefix, dst_row, recv_src, expert_ids, usage, total;
+};
+
+Carve carve_of(const ep_params* p) {
+    const Tiling t = tiling_of(p);
+    const int64_t R = p->num_ranks, E = p->num_experts, L = E / R;
+    const int64_t N = R * p->tokens_per_rank, K = p->topk;
+    Carve c;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + (bytes ? bytes : 1)); return o; };
+    c.status = take(sizeof(int32_t));
+    c.blk_hist = take(sizeof(int32_t) * (size_t)t.B * E);
+    c.blk_rank = take(sizeof(int32_t) * (size_t)t.B * R);
+    c.cnt = take(sizeof(int32_t) * (size_t)(R * E));
+    c.itr = take((size_t)(N * R));
+    c.ntpr = take(sizeof(int32_t) * (size_t)(R * R));
+    c.recv_cnt = take(sizeof(int32_t) * (size_t)E);
+    c.aligned = take(sizeof(int32_t) * (size_t)E);
+    c.expert_start = take(sizeof(int32_t) * (size_t)(R * (L + 1)));
+    c.rank_base = take(sizeof(int64_t) * (size_t)(R + 1));
+    c.expert_base = take(sizeof(int32_t) * (size_t)(E + 1));
+    c.src_prefix = take(sizeof(int32_t) * (size_t)(R * E));
+    c.dst_row = take(sizeof(int32_t) * (size_t)(N * K));
+    c.recv_src = take(sizeof(int32_t) * (size_t)recv_cap_of(p));
+    c.expert_ids = take(sizeof(int32_t) * (size_t)(R * L));
+    c.usage = take(sizeof(int32_t) * (size_t)(R * 2));
+    c.total = off;
+    return c;
+}
+
+ep_status from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+int ep_device_sms(ep_handle* h) {
+    if (h->num_sms > 0) return h->num_sms;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    h->device = dev;
+    h->num_sms = sms;
+    return sms;
+}
+
+extern "C" {
+
+const char* ep_status_string(ep_status s) {
+    switch (s) {
+        case EP_OK: return "EP_OK";
+        case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+        case EP_ERR_UNSUPPORTED: return "EP_ERR_UNSUPPORTED";
+        case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
+        case EP_ERR_BAD_EXPERT_ID: return "EP_ERR_BAD_EXPERT_ID";
+        case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+        case EP_ERR_CUDA: return "EP_ERR_CUDA";
+    }
+    return "EP_ERR_UNKNOWN";
+}
+
+ep_status ep_params_validate(const ep_params* p) {
+    if (!p) return EP_ERR_INVALID_ARG;
+    if (p->num_ranks < 1) return EP_ERR_INVALID_ARG;
+    if (p->num_experts < 1 || p->num_experts > kMaxExperts) return EP_ERR_INVALID_ARG;
+    if (p->num_experts % p->num_ranks != 0) return EP_ERR_INVALID_ARG;
+    if (p->topk < 1 || p->topk > kMaxTopk || p->topk > p->num_experts) return EP_ERR_INVALID_ARG;
+    if (p->tokens_per_rank < 0 || p->tokens_per_rank > 65536) return EP_ERR_INVALID_ARG;
+    if (p->hidden < 8 || p->hidden > 8192 || p->hidden % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (p->expert_alignment < 1 || p->expert_alignment > 4096) return EP_ERR_INVALID_ARG;
+    if (p->recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
+    if (worst_rows(p) >= (int64_t)INT32_MAX || p->recv_capacity_rows >= (int64_t)INT32_MAX)
+        return EP_ERR_INVALID_ARG;
+    return EP_OK;
+}
+
+ep_status ep_layout_workspace_size(const ep_params* p, size_t* bytes) {
+    ep_status s = ep_params_validate(p);
+    if (s != EP_OK) return s;
+    if (!bytes) return EP_ERR_INVALID_ARG;
+    *bytes = carve_of(p).total;
+    return EP_OK;
+}
+
+ep_status ep_recv_row_bytes(int32_t hidden, ep_quant_mode q, int64_t* data_bytes, int64_t* scale_bytes) {
+    if (!data_bytes || !scale_bytes) return EP_ERR_INVALID_ARG;
+    if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (is_mx(q) && hidden % 32 != 0) return EP_ERR_INVALID_ARG;
+    switch (q) {
+        case EP_QUANT_NONE: *data_bytes = 2 * (int64_t)hidden; *scale_bytes = 0; break;
+        case EP_QUANT_INT8_PER_TOKEN: *data_bytes = hidden; *scale_bytes = 4; break;
+        case EP_QUANT_MXFP8_E4M3:
+        case EP_QUANT_MXFP8_E5M2: *data_bytes = hidden; *scale_bytes = hidden / 32; break;
+        case EP_QUANT_MXFP4_E2M1: *data_bytes = hidden / 2; *scale_bytes = hidden / 32; break;
+    }
+    return EP_OK;
+}
+
+ep_status ep_handle_create(const ep_params* p, void* workspace, size_t workspace_bytes, ep_handle** out) {
+    ep_status s = ep_params_validate(p);
+    if (s != EP_OK) return s;
+    if (!out || !workspace || !aligned_to(workspace, kAlign)) return EP_ERR_INVALID_ARG;
+    const Carve c = carve_of(p);
+    if (workspace_bytes < c.total) return EP_ERR_INVALID_ARG;
+    ep_handle* h = (ep_handle*)calloc(1, sizeof(ep_handle));
+    if (!h) return EP_ERR_INVALID_ARG;
+    const Tiling t = tiling_of(p);
+    h->p = *p;
+    h->R = p->num_ranks; h->T = p->tokens_per_rank; h->H = p->hidden; h->E = p->num_experts;
+    h->K = p->topk; h->L = p->num_experts / p->num_ranks; h->alpha = p->expert_alignment;
+    h->N = (int64_t)h->R * h->T;
+    h->recv_cap = recv_cap_of(p);
+    h->C = t.C; h->TPB = t.TPB; h->B = t.B;
+    h->ws = workspace; h->ws_bytes = workspace_bytes;
+    uint8_t* w = (uint8_t*)workspace;
+    h->status = (int32_t*)(w + c.status);
+    h->blk_hist = (int32_t*)(w + c.blk_hist);
+    h->blk_rank = (int32_t*)(w + c.blk_rank);
+    h->cnt = (int32_t*)(w + c.cnt);
+    h->itr = (uint8_t*)(w + c.itr);
+    h->ntpr = (int32_t*)(w + c.ntpr);
+    h->recv_cnt = (int32_t*)(w + c.recv_cnt);
+    h->aligned = (int32_t*)(w + c.aligned);
+    h->expert_start = (int32_t*)(w + c.expert_start);
+    h->rank_base = (int64_t*)(w + c.rank_base);
+    h->expert_base = (int32_t*)(w + c.expert_base);
+    h->src_prefix = (int32_t*)(w + c.src_prefix);
+    h->dst_row = (int32_t*)(w + c.dst_row);
+    h->recv_src = (int32_t*)(w + c.recv_src);
+    h->expert_ids = (int32_t*)(w + c.expert_ids);
+    h->usage = (int32_t*)(w + c.usage);
+    *out = h;
+    return EP_OK;
+}
+
+ep_status ep_handle_destroy(ep_handle* h) {
+    free(h);
+    return EP_OK;
+}
+
+ep_status ep_layout(ep_handle* h, const int64_t* topk, ep_stream_t stream) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (h->N > 0 && (!topk || !aligned_to(topk, 8))) return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    return from_cuda(launch_layout(h, topk, (cudaStream_t)stream));
+}
+
+ep_status ep_handle_views(const ep_handle* h, ep_layout_views* v) {
+    if (!h || !v) return EP_ERR_INVALID_ARG;
+    v->cnt = h->cnt;
+    v->is_token_in_rank = h->itr;
+    v->num_tokens_per_rank = h->ntpr;
+    v->recv_cnt = h->recv_cnt;
+    v->aligned_cnt = h->aligned;
+    v->expert_start = h->expert_start;
+    v->rank_base = h->rank_base;
+    v->expert_base = h->expert_base;
+    v->src_prefix = h->src_prefix;
+    v->dst_row = h->dst_row;
+    v->recv_src = h->recv_src;
+    v->expert_ids = h->expert_ids;
+    v->expert_usage_stats = h->usage;
+    v->recv_src_capacity = h->recv_cap;
+    return EP_OK;
+}
+
+ep_status ep_handle_recv_rows(const ep_handle* h, int64_t* host, ep_stream_t stream) {
+    if (!h || !host) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
+    return from_cuda(cudaMemcpy(host, h->rank_base, sizeof(int64_t) * (size_t)(h->R + 1),
+                                cudaMemcpyDeviceToHost));
+}
+
+ep_status ep_handle_expert_counts(const ep_handle* h, int32_t* host, ep_stream_t stream) {
+    if (!h || !host) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
+    return from_cuda(cudaMemcpy(host, h->aligned, sizeof(int32_t) * (size_t)h->E,
+                                cudaMemcpyDeviceToHost));
+}
+
+ep_status ep_handle_status(const ep_handle* h, ep_stream_t stream) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return EP_ERR_CUDA;
+    return (ep_status)v;
+}
+
+ep_status ep_dispatch(const ep_handle* hc, const void* x, ep_quant_mode q, void* recv_data,
+                      void* recv_scales, int64_t cap, ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    if (is_mx(q) && h->H % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (cap < 0) return EP_ERR_INVALID_ARG;
+    if (h->N > 0 && (!x || !aligned_to(x, 16))) return EP_ERR_INVALID_ARG;
+    if (!recv_data && cap > 0) return EP_ERR_INVALID_ARG;
+    if (recv_data && !aligned_to(recv_data, 16)) return EP_ERR_INVALID_ARG;
+    if (q != EP_QUANT_NONE && cap > 0 && (!recv_scales || !aligned_to(recv_scales, 4)))
+        return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    int64_t db = 0, sb = 0;
+    ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);
+    if (s != EP_OK) return s;
+    DispatchArgs a;
+    a.x = (const uint16_t*)x;
+    a.data = (uint8_t*)recv_data;
+    a.scales = (uint8_t*)recv_scales;
+    a.dst_row = h->dst_row;
+    a.expert_base = h->expert_base;
+    a.recv_cnt = h->recv_cnt;
+    a.status = h->status;
+    a.N = h->N;
+    a.cap = cap;
+    a.H = h->H; a.K = h->K; a.E = h->E; a.nvec = h->H / 8;
+    a.row_bytes = (int32_t)db;
+    a.scale_bytes = (int32_t)sb;
+    return from_cuda(launch_dispatch(h, a, (int)q, (cudaStream_t)stream));
+}
+
+ep_status ep_combine(const ep_handle* hc, const void* y, int64_t y_cap, const float* w,
+                     const void* shared, int32_t S, void* out, ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (S < 0 || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
+    if (y_cap < 0) return EP_ERR_INVALID_ARG;
+    if (h->N > 0) {
+        if (!w || !aligned_to(w, 4) || !out || !aligned_to(out, 16)) return EP_ERR_INVALID_ARG;
+        if (y_cap > 0 && (!y || !aligned_to(y, 16))) return EP_ERR_INVALID_ARG;
+    }
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    CombineArgs a;
+    a.y = (const uint16_t*)y;
+    a.w = w;
+    a.shared = (const uint16_t*)shared;
+    a.out = (uint16_t*)out;
+    a.dst_row = h->dst_row;
+    a.expert_base = h->expert_base;
+    a.status = h->status;
+    a.N = h->N;
+    a.cap = y_cap;
+    a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
+    return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
+}
+
+ep_status ep_expert_identity(const ep_handle* hc, ep_quant_mode q, const void* recv_data,
+                             const void* recv_scales, int64_t cap, int32_t mark_mod, void* y,
+                             ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    if (is_mx(q) && h->H % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (cap < 0 || mark_mod < 0) return EP_ERR_INVALID_ARG;
+    if (cap > 0 && (!recv_data || !y || !aligned_to(y, 4))) return EP_ERR_INVALID_ARG;
+    if (q != EP_QUANT_NONE && cap > 0 && !recv_scales) return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    int64_t db = 0, sb = 0;
+    ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);
+    if (s != EP_OK) return s;
+    IdentityArgs a;
+    a.data = (const uint8_t*)recv_data;
+    a.scales = (const uint8_t*)recv_scales;
+    a.y = (uint16_t*)y;
+    a.expert_base = h->expert_base;
+    a.recv_src = h->recv_src;
+    a.status = h->status;
+    a.cap = cap;
+    a.recv_src_cap = h->recv_cap;
+    a.H = h->H; a.E = h->E; a.nvec = h->H / 8;
+    a.row_bytes = (int32_t)db; a.scale_bytes = (int32_t)sb; a.mark_mod = mark_mod;
+    return from_cuda(launch_identity(h, a, (int)q, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+// ep_internal.cuh -- internal declarations of libeplayout (host bookkeeping,
+// kernel argument blocks, launch helpers).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep_layout.h"
+
+// Layout tiling: each layout CTA owns a contiguous range of one source rank's
+// tokens, so per-CTA histograms can be summed into per-rank counts.
+constexpr int kLayoutThreads = 256;
+constexpr int kLayoutTargetBlocks = 608;  // 4 x 152 SMs; fixes the workspace size
+constexpr int kMaxTopk = 16;
+constexpr int kMaxExperts = 512;
+
+struct ep_handle {
+    ep_params p;
+    int32_t R, T, H, E, K, L, alpha;
+    int64_t N;          // R * T source tokens
+    int64_t recv_cap;   // rows of recv_src
+    int32_t C;          // layout CTAs per source rank
+    int32_t TPB;        // tokens per layout CTA
+    int32_t B;          // layout CTAs = R * C
+    void* ws;
+    size_t ws_bytes;
+    int device;
+    int num_sms;        // 0 until the first launch queries it
+    // device arrays inside the workspace
+    int32_t* status;
+    int32_t* blk_hist;      // [B][E] per-CTA expert counts, then per-CTA exclusive prefixes
+    int32_t* blk_rank;      // [B][R] per-CTA tokens per destination rank
+    int32_t* cnt;           // [R][E]
+    uint8_t* itr;           // [N][R]
+    int32_t* ntpr;          // [R][R]
+    int32_t* recv_cnt;      // [E]
+    int32_t* aligned;       // [E]
+    int32_t* expert_start;  // [R][L+1]
+    int64_t* rank_base;     // [R+1]
+    int32_t* expert_base;   // [E+1]
+    int32_t* src_prefix;    // [R][E]
+    int32_t* dst_row;       // [N][K]
+    int32_t* recv_src;      // [recv_cap]
+    int32_t* expert_ids;    // [R][L]
+    int32_t* usage;         // [R][2]
+};
+
+// Argument block shared by the three layout kernels.
+struct LayoutArgs {
+    const int64_t* topk;
+    int32_t R, T, E, K, L, alpha, C, TPB, B;
+    int64_t recv_cap;
+    int32_t* status;
+    int32_t* blk_hist;
+    int32_t* blk_rank;
+    int32_t* cnt;
+    uint8_t* itr;
+    int32_t* ntpr;
+    int32_t* recv_cnt;
+    int32_t* aligned;
+    int32_t* expert_start;
+    int64_t* rank_base;
+    int32_t* expert_base;
+    int32_t* src_prefix;
+    int32_t* dst_row;
+    int32_t* recv_src;
+    int32_t* expert_ids;
+    int32_t* usage;
+};
+
+struct DispatchArgs {
+    const uint16_t* x;        // [N][H] bf16
+    uint8_t* data;            // [cap][row_bytes]
+    uint8_t* scales;          // [cap][scale_bytes] or null
+    const int32_t* dst_row;   // [N][K]
+    const int32_t* expert_base;
+    const int32_t* recv_cnt;
+    int32_t* status;
+    int64_t N;
+    int64_t cap;
+    int32_t H, K, E, nvec;    // nvec = H / 8 (16-byte vectors per bf16 row)
+    int32_t row_bytes, scale_bytes;
+};
+
+struct CombineArgs {
+    const uint16_t* y;        // [cap][H] bf16
+    const float* w;           // [N][K]
+    const uint16_t* shared;   // [R][S][T][H] bf16 or null
+    uint16_t* out;            // [N][H]
+    const int32_t* dst_row;
+    const int32_t* expert_base;
+    int32_t* status;
+    int64_t N;
+    int64_t cap;
+    int32_t T, H, K, E, S, nvec;
+};
+
+struct IdentityArgs {
+    const uint8_t* data;
+    const uint8_t* scales;
+    uint16_t* y;
+    const int32_t* expert_base;
+    const int32_t* recv_src;
+    int32_t* status;
+    int64_t cap;
+    int64_t recv_src_cap;
+    int32_t H, E, nvec, row_bytes, scale_bytes, mark_mod;
+};
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, cudaStream_t st);
+cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st);
+cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st);
+cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant, cudaStream_t st);
+
+// Device helpers shared by the kernels of this library.
+__device__ __forceinline__ void ep_set_status(int32_t* status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
+    return __uint_as_float(b16 << 16);
+}
+
+// Round-to-nearest-even float32 pair -> packed bf16x2 (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_u32(void* p, uint32_t v) {
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+int ep_device_sms(ep_handle* h);

@@ -1,0 +1,290 @@
+// layout.cu -- routing layout from topk_idx (DeepEP "Normal Mode API" layout
+// inputs; CANN aclnnMoeDistributeDispatchV2 expert placement; MAX
+// EPBatchManager.ep_dispatch expert_start_indices / expert_usage_stats).
+//
+// Three kernels, no inter-CTA waiting:
+//   count  - per CTA (a contiguous token range of one source rank): expert
+//            histogram in shared memory, is_token_in_rank (one warp per token),
+//            tokens per destination rank.
+//   scan   - per expert column: exclusive prefix of the CTA histograms over
+//            CTAs (global order = source rank, then token), per-source-rank
+//            counts and prefixes, received totals; num_tokens_per_rank.
+//   assign - per CTA: exclusive scan of the aligned counts (expert bases),
+//            then a warp-ordered pass: __match_any_sync ranks equal experts
+//            inside each 32-entry step, per-warp running counters keep the
+//            (token, slot) order, so every receive row is fixed without
+//            atomics.  CTA 0 writes the per-rank metadata.
+#include "ep_internal.cuh"
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_count_kernel(LayoutArgs a) {
+    extern __shared__ int smem[];
+    int* hist = smem;          // [E]
+    int* rcnt = smem + a.E;    // [R]
+    const int b = blockIdx.x;
+    const int s = b / a.C, c = b - (b / a.C) * a.C;
+    const int t0 = c * a.TPB;
+    const int t1 = min(a.T, t0 + a.TPB);
+    for (int i = threadIdx.x; i < a.E + a.R; i += blockDim.x) smem[i] = 0;
+    __syncthreads();
+
+    const int64_t n0 = (int64_t)s * a.T;
+    bool bad = false;
+    if (t1 > t0) {
+        const int64_t ebeg = (n0 + t0) * a.K, eend = (n0 + t1) * a.K;
+        for (int64_t i = ebeg + threadIdx.x; i < eend; i += blockDim.x) {
+            const int64_t e = a.topk[i];
+            if (e == -1) continue;
+            if (e < -1 || e >= a.E) { bad = true; continue; }
+            atomicAdd(&hist[(int)e], 1);
+        }
+        // is_token_in_rank: one warp per token, lanes over destination ranks
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int nwarps = blockDim.x >> 5;
+        for (int t = t0 + warp; t < t1; t += nwarps) {
+            const int64_t n = n0 + t;
+            int rk = -1;
+            if (lane < a.K) {
+                const int64_t e = a.topk[n * a.K + lane];
+                if (e >= 0 && e < a.E) rk = (int)e / a.L;
+            }
+            for (int j0 = 0; j0 < a.R; j0 += 32) {
+                const int j = j0 + lane;
+                bool hit = false;
+                for (int kk = 0; kk < a.K; ++kk) hit |= (__shfl_sync(kFull, rk, kk) == j);
+                if (j < a.R) {
+                    a.itr[n * a.R + j] = hit ? 1 : 0;
+                    if (hit) atomicAdd(&rcnt[j], 1);
+                }
+            }
+        }
+    }
+    if (bad) ep_set_status(a.status, EP_ERR_BAD_EXPERT_ID);
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.blk_hist[(int64_t)b * a.E + e] = hist[e];
+    for (int j = threadIdx.x; j < a.R; j += blockDim.x) a.blk_rank[(int64_t)b * a.R + j] = rcnt[j];
+}
+
+// 32 expert columns per CTA; 32 row slices of the CTA-histogram matrix each.
+__global__ void __launch_bounds__(1024)
+layout_scan_kernel(LayoutArgs a) {
+    __shared__ int part[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + tx;
+    const int per = (a.B + 31) / 32;
+    const int b0 = min(a.B, ty * per), b1 = min(a.B, b0 + per);
+    int sum = 0;
+    if (e < a.E)
+        for (int b = b0; b < b1; ++b) sum += a.blk_hist[(int64_t)b * a.E + e];
+    part[ty][tx] = sum;
+    __syncthreads();
+    if (ty == 0) {
+        int run = 0;
+        for (int i = 0; i < 32; ++i) {
+            const int v = part[i][tx];
+            part[i][tx] = run;
+            run += v;
+        }
+        if (e < a.E) a.recv_cnt[e] = run;
+    }
+    __syncthreads();
+    if (e < a.E) {
+        int run = part[ty][tx];
+        for (int b = b0; b < b1; ++b) {
+            const int64_t idx = (int64_t)b * a.E + e;
+            const int v = a.blk_hist[idx];
+            a.blk_hist[idx] = run;
+            if (b % a.C == 0) a.src_prefix[(int64_t)(b / a.C) * a.E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    if (e < a.E) {
+        for (int s = ty; s < a.R; s += 32) {
+            const int next = (s + 1 < a.R) ? a.src_prefix[(int64_t)(s + 1) * a.E + e] : a.recv_cnt[e];
+            a.cnt[(int64_t)s * a.E + e] = next - a.src_prefix[(int64_t)s * a.E + e];
+        }
+    }
+    // num_tokens_per_rank[s][j] = sum over the rank's CTAs
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t gsz = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g = gid; g < (int64_t)a.R * a.R; g += gsz) {
+        const int s = (int)(g / a.R), j = (int)(g - (int64_t)s * a.R);
+        int acc = 0;
+        for (int c = 0; c < a.C; ++c) acc += a.blk_rank[((int64_t)s * a.C + c) * a.R + j];
+        a.ntpr[g] = acc;
+    }
+}
+
+// Exclusive scan of vals[0..n) into out[0..n] (out[n] = total), one CTA.
+// scratch needs blockDim.x / 32 + 1 ints.
+__device__ void block_exclusive_scan(const int* vals, int* out, int n, int* scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int chunk = (n + nt - 1) / nt;
+    const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) local += vals[i];
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < (nt >> 5); ++w) {
+            const int v = scratch[w];
+            scratch[w] = run;
+            run += v;
+        }
+        scratch[nt >> 5] = run;
+    }
+    __syncthreads();
+    int run = scratch[warp] + incl - local;
+    for (int i = i0; i < i1; ++i) {
+        out[i] = run;
+        run += vals[i];
+    }
+    if (tid == 0) out[n] = scratch[nt >> 5];
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_assign_kernel(LayoutArgs a) {
+    extern __shared__ int smem[];
+    constexpr int NW = kLayoutThreads / 32;
+    const int E = a.E;
+    int* rc = smem;                 // [E] received counts
+    int* al = rc + E;               // [E] aligned counts
+    int* base = al + E;             // [E+1] first global row of each expert
+    int* scratch = base + E + 1;    // [NW+1]
+    int* wc = scratch + NW + 1;     // [NW][E] per-warp running rows
+
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int c = a.recv_cnt[e];
+        rc[e] = c;
+        al[e] = ((c + a.alpha - 1) / a.alpha) * a.alpha;
+    }
+    __syncthreads();
+    block_exclusive_scan(al, base, E, scratch);
+
+    const int b = blockIdx.x;
+    const int64_t cap = a.recv_cap;
+    if (b == 0) {
+        const int L = a.L;
+        for (int e = tid; e < E; e += blockDim.x) {
+            a.aligned[e] = al[e];
+            a.expert_base[e] = base[e];
+        }
+        if (tid == 0) {
+            a.expert_base[E] = base[E];
+            a.rank_base[a.R] = base[E];
+            if ((int64_t)base[E] > cap) ep_set_status(a.status, EP_ERR_CAPACITY);
+        }
+        for (int j = tid; j < a.R; j += blockDim.x) {
+            a.rank_base[j] = base[j * L];
+            int mx = 0, act = 0;
+            for (int l = 0; l < L; ++l) {
+                mx = max(mx, al[j * L + l]);
+                act += rc[j * L + l] > 0 ? 1 : 0;
+            }
+            a.usage[2 * j] = mx;
+            a.usage[2 * j + 1] = act;
+        }
+        for (int i = tid; i < a.R * (L + 1); i += blockDim.x) {
+            const int j = i / (L + 1), l = i - j * (L + 1);
+            a.expert_start[i] = base[j * L + l] - base[j * L];
+        }
+        for (int i = tid; i < a.R * L; i += blockDim.x) a.expert_ids[i] = i % L;
+    }
+    // padding rows of the experts this CTA owns
+    for (int e = b; e < E; e += gridDim.x) {
+        const int64_t r1 = min((int64_t)base[e + 1], cap);
+        for (int64_t r = (int64_t)base[e] + rc[e] + tid; r < r1; r += blockDim.x) a.recv_src[r] = -1;
+    }
+
+    const int s = b / a.C, c = b - (b / a.C) * a.C;
+    const int t0 = c * a.TPB;
+    const int t1 = min(a.T, t0 + a.TPB);
+    if (t1 <= t0) return;
+    const int64_t ebeg = ((int64_t)s * a.T + t0) * a.K;
+    const int M = (t1 - t0) * a.K;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int per = ((M + NW - 1) / NW + 31) & ~31;
+    const int w0 = min(M, warp * per), w1 = min(M, w0 + per);
+    int* mycnt = wc + warp * E;
+
+    // phase A: per-warp expert counts over the warp's entry range
+    for (int e = lane; e < E; e += 32) mycnt[e] = 0;
+    __syncwarp();
+    for (int i = w0 + lane; i < w1; i += 32) {
+        const int64_t e = a.topk[ebeg + i];
+        if (e >= 0 && e < E) atomicAdd(&mycnt[(int)e], 1);
+    }
+    __syncthreads();
+    // phase B: first row of each (warp, expert) = expert base + CTA prefix + earlier warps
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = base[e] + a.blk_hist[(int64_t)b * E + e];
+        for (int w = 0; w < NW; ++w) {
+            const int v = wc[w * E + e];
+            wc[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    // phase C: ordered walk; equal experts inside a step are ranked by lane
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        int e = -1;
+        if (i < w1) {
+            const int64_t ev = a.topk[ebeg + i];
+            if (ev >= 0 && ev < E) e = (int)ev;
+        }
+        const unsigned peers = __match_any_sync(kFull, e);
+        int pos = -1;
+        if (e >= 0) pos = mycnt[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) mycnt[e] += __popc(peers);
+        __syncwarp();
+        if (i < w1) {
+            a.dst_row[ebeg + i] = pos;
+            if (pos >= 0 && (int64_t)pos < cap) a.recv_src[pos] = (int32_t)((ebeg + i) / a.K);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, cudaStream_t st) {
+    LayoutArgs a;
+    a.topk = topk;
+    a.R = h->R; a.T = h->T; a.E = h->E; a.K = h->K; a.L = h->L; a.alpha = h->alpha;
+    a.C = h->C; a.TPB = h->TPB; a.B = h->B;
+    a.recv_cap = h->recv_cap;
+    a.status = h->status;
+    a.blk_hist = h->blk_hist; a.blk_rank = h->blk_rank; a.cnt = h->cnt; a.itr = h->itr;
+    a.ntpr = h->ntpr; a.recv_cnt = h->recv_cnt; a.aligned = h->aligned;
+    a.expert_start = h->expert_start; a.rank_base = h->rank_base; a.expert_base = h->expert_base;
+    a.src_prefix = h->src_prefix; a.dst_row = h->dst_row; a.recv_src = h->recv_src;
+    a.expert_ids = h->expert_ids; a.usage = h->usage;
+
+    cudaError_t err = cudaMemsetAsync(h->status, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+    const size_t smem_count = sizeof(int) * (size_t)(h->E + h->R);
+    layout_count_kernel<<<h->B, kLayoutThreads, smem_count, st>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    layout_scan_kernel<<<(h->E + 31) / 32, 1024, 0, st>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    constexpr int NW = kLayoutThreads / 32;
+    const size_t smem_assign = sizeof(int) * (size_t)(3 * h->E + 1 + NW + 1 + NW * h->E);
+    layout_assign_kernel<<<h->B, kLayoutThreads, smem_assign, st>>>(a);
+    return cudaGetLastError();
+}

@@ -1,0 +1,292 @@
+"""Thin Python binding of libeplayout.so (the C ABI in include/ep_layout.h).
+
+Argument marshalling only: torch tensors supply device memory and streams,
+every step of layout / dispatch / combine runs in the library's CUDA kernels.
+Importing this module loads the library and raises ImportError when it has not
+been built (``python -m combine_ep_layout_03_gb300.build``); there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libeplayout.so")
+
+EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CAPACITY = 0, 1, 2, 3
+EP_ERR_BAD_EXPERT_ID, EP_ERR_TIMEOUT, EP_ERR_CUDA = 4, 5, 6
+
+EP_QUANT_NONE = 0
+EP_QUANT_INT8_PER_TOKEN = 2
+EP_QUANT_MXFP8_E4M3 = 4
+EP_QUANT_MXFP8_E5M2 = 5
+EP_QUANT_MXFP4_E2M1 = 6
+QUANT_MODES = (EP_QUANT_NONE, EP_QUANT_INT8_PER_TOKEN, EP_QUANT_MXFP8_E4M3,
+               EP_QUANT_MXFP8_E5M2, EP_QUANT_MXFP4_E2M1)
+
+
+class EPError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{what}: {status_string(status)}" if what else status_string(status))
+
+
+class ep_params(ctypes.Structure):
+    _fields_ = [("num_ranks", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("expert_alignment", ctypes.c_int32),
+                ("recv_capacity_rows", ctypes.c_int64)]
+
+
+class ep_layout_views(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt", "aligned_cnt",
+        "expert_start", "rank_base", "expert_base", "src_prefix", "dst_row", "recv_src",
+        "expert_ids", "expert_usage_stats")] + [("recv_src_capacity", ctypes.c_int64)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libeplayout.so is not built ({LIB_PATH}); run "
+                          "`python -m combine_ep_layout_03_gb300.build` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+    P = ctypes.POINTER(ep_params)
+    sig = {
+        "ep_status_string": ([st], ctypes.c_char_p),
+        "ep_params_validate": ([P], st),
+        "ep_layout_workspace_size": ([P, ctypes.POINTER(ctypes.c_size_t)], st),
+        "ep_recv_row_bytes": ([i32, st, ctypes.POINTER(i64), ctypes.POINTER(i64)], st),
+        "ep_handle_create": ([P, vp, ctypes.c_size_t, ctypes.POINTER(vp)], st),
+        "ep_handle_destroy": ([vp], st),
+        "ep_layout": ([vp, vp, vp], st),
+        "ep_handle_views": ([vp, ctypes.POINTER(ep_layout_views)], st),
+        "ep_handle_recv_rows": ([vp, vp, vp], st),
+        "ep_handle_expert_counts": ([vp, vp, vp], st),
+        "ep_handle_status": ([vp, vp], st),
+        "ep_dispatch": ([vp, vp, st, vp, vp, i64, vp], st),
+        "ep_combine": ([vp, vp, i64, vp, vp, i32, vp, vp], st),
+        "ep_expert_identity": ([vp, st, vp, vp, i64, i32, vp, vp], st),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+lib = _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.ep_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != EP_OK:
+        raise EPError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_params(R, T, H, E, K, alpha=1, recv_capacity_rows=0) -> ep_params:
+    return ep_params(R, T, H, E, K, alpha, recv_capacity_rows)
+
+
+# ---------------------------------------------------------------- C-named calls
+
+def ep_params_validate(p: ep_params) -> int:
+    return _lib.ep_params_validate(ctypes.byref(p))
+
+
+def ep_layout_workspace_size(p: ep_params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.ep_layout_workspace_size(ctypes.byref(p), ctypes.byref(n)), "ep_layout_workspace_size")
+    return int(n.value)
+
+
+def ep_recv_row_bytes(hidden: int, quant: int) -> tuple[int, int]:
+    d, s = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(_lib.ep_recv_row_bytes(hidden, quant, ctypes.byref(d), ctypes.byref(s)), "ep_recv_row_bytes")
+    return int(d.value), int(s.value)
+
+
+def ep_handle_create(p: ep_params, workspace: torch.Tensor) -> int:
+    h = ctypes.c_void_p(0)
+    _check(_lib.ep_handle_create(ctypes.byref(p), workspace.data_ptr(), workspace.numel(),
+                                 ctypes.byref(h)), "ep_handle_create")
+    return int(h.value)
+
+
+def ep_handle_destroy(h: int) -> None:
+    _lib.ep_handle_destroy(h)
+
+
+def ep_layout(h: int, topk_idx: torch.Tensor, stream=None) -> None:
+    _check(_lib.ep_layout(h, _ptr(topk_idx), _stream(stream)), "ep_layout")
+
+
+def ep_handle_views(h: int) -> ep_layout_views:
+    v = ep_layout_views()
+    _check(_lib.ep_handle_views(h, ctypes.byref(v)), "ep_handle_views")
+    return v
+
+
+def ep_handle_recv_rows(h: int, R: int, stream=None) -> list[int]:
+    buf = (ctypes.c_int64 * (R + 1))()
+    _check(_lib.ep_handle_recv_rows(h, ctypes.addressof(buf), _stream(stream)), "ep_handle_recv_rows")
+    return list(buf)
+
+
+def ep_handle_expert_counts(h: int, E: int, stream=None) -> list[int]:
+    buf = (ctypes.c_int32 * E)()
+    _check(_lib.ep_handle_expert_counts(h, ctypes.addressof(buf), _stream(stream)),
+           "ep_handle_expert_counts")
+    return list(buf)
+
+
+def ep_handle_status(h: int, stream=None) -> int:
+    return int(_lib.ep_handle_status(h, _stream(stream)))
+
+
+def ep_dispatch(h: int, x, quant: int, recv_data, recv_scales, recv_rows_capacity: int,
+                stream=None) -> None:
+    _check(_lib.ep_dispatch(h, _ptr(x), quant, _ptr(recv_data), _ptr(recv_scales),
+                            int(recv_rows_capacity), _stream(stream)), "ep_dispatch")
+
+
+def ep_combine(h: int, y, y_rows_capacity: int, topk_weights, shared, num_shared: int, out,
+               stream=None) -> None:
+    _check(_lib.ep_combine(h, _ptr(y), int(y_rows_capacity), _ptr(topk_weights), _ptr(shared),
+                           int(num_shared), _ptr(out), _stream(stream)), "ep_combine")
+
+
+def ep_expert_identity(h: int, quant: int, recv_data, recv_scales, rows_capacity: int,
+                       mark_mod: int, y, stream=None) -> None:
+    _check(_lib.ep_expert_identity(h, quant, _ptr(recv_data), _ptr(recv_scales),
+                                   int(rows_capacity), int(mark_mod), _ptr(y), _stream(stream)),
+           "ep_expert_identity")
+
+
+# ---------------------------------------------------------------- convenience wrapper
+
+_VIEW_SPECS = {
+    # name: (dtype, shape builder)
+    "cnt": (torch.int32, lambda s: (s.R, s.E)),
+    "is_token_in_rank": (torch.uint8, lambda s: (s.R, s.T, s.R)),
+    "num_tokens_per_rank": (torch.int32, lambda s: (s.R, s.R)),
+    "recv_cnt": (torch.int32, lambda s: (s.E,)),
+    "aligned_cnt": (torch.int32, lambda s: (s.R, s.L)),
+    "expert_start": (torch.int32, lambda s: (s.R, s.L + 1)),
+    "rank_base": (torch.int64, lambda s: (s.R + 1,)),
+    "expert_base": (torch.int32, lambda s: (s.E + 1,)),
+    "src_prefix": (torch.int32, lambda s: (s.R, s.E)),
+    "dst_row": (torch.int32, lambda s: (s.R, s.T, s.K)),
+    "recv_src": (torch.int32, lambda s: (s.recv_src_capacity,)),
+    "expert_ids": (torch.int32, lambda s: (s.R, s.L)),
+    "expert_usage_stats": (torch.int32, lambda s: (s.R, 2)),
+}
+
+
+class EPLayout:
+    """A handle plus its device workspace (a torch uint8 tensor).
+
+    ``layout(topk_idx)`` fills the handle; ``views()`` exposes the layout arrays
+    as torch tensors aliasing the workspace; ``dispatch`` / ``combine`` run the
+    kernels on caller tensors.  R logical ranks share one GPU."""
+
+    def __init__(self, R, T, H, E, K, alpha=1, recv_capacity_rows=0, device="cuda"):
+        self.R, self.T, self.H, self.E, self.K, self.alpha = R, T, H, E, K, alpha
+        self.L = E // R
+        self.params = make_params(R, T, H, E, K, alpha, recv_capacity_rows)
+        nbytes = ep_layout_workspace_size(self.params)
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.workspace.data_ptr()) % 256
+        self.ws = self.workspace[off:off + nbytes]
+        self.h = ep_handle_create(self.params, self.ws)
+        self.recv_src_capacity = ep_handle_views(self.h).recv_src_capacity
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            ep_handle_destroy(h)
+            self.h = None
+
+    @property
+    def worst_rows(self) -> int:
+        return self.R * self.T * self.K + self.E * (self.alpha - 1)
+
+    def layout(self, topk_idx: torch.Tensor, stream=None) -> "EPLayout":
+        assert topk_idx.dtype == torch.int64 and topk_idx.is_contiguous()
+        assert topk_idx.numel() == self.R * self.T * self.K
+        ep_layout(self.h, topk_idx, stream)
+        return self
+
+    def views(self) -> dict[str, torch.Tensor]:
+        v = ep_handle_views(self.h)
+        base = self.ws.data_ptr()
+        out = {}
+        for name, (dt, shape) in _VIEW_SPECS.items():
+            shp = shape(self)
+            n = 1
+            for d in shp:
+                n *= d
+            off = getattr(v, name) - base
+            nbytes = n * torch.empty((), dtype=dt).element_size()
+            out[name] = self.ws[off:off + nbytes].view(dt).view(shp)
+        return out
+
+    def recv_rows(self, stream=None) -> list[int]:
+        """rank_base on the host (synchronises the stream)."""
+        return ep_handle_recv_rows(self.h, self.R, stream)
+
+    def expert_counts(self, stream=None) -> list[int]:
+        return ep_handle_expert_counts(self.h, self.E, stream)
+
+    def status(self, stream=None) -> int:
+        return ep_handle_status(self.h, stream)
+
+    def alloc_recv(self, quant: int, rows: int | None = None, device="cuda"):
+        rows = self.worst_rows if rows is None else rows
+        db, sb = ep_recv_row_bytes(self.H, quant)
+        data = torch.empty((rows, db), dtype=torch.uint8, device=device)
+        scales = torch.empty((rows, sb), dtype=torch.uint8, device=device) if sb else None
+        return data, scales
+
+    def dispatch(self, x: torch.Tensor, quant: int, recv_data: torch.Tensor,
+                 recv_scales: torch.Tensor | None, stream=None) -> None:
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        cap = recv_data.numel() // db
+        ep_dispatch(self.h, x, quant, recv_data, recv_scales, cap, stream)
+
+    def combine(self, y: torch.Tensor, topk_weights: torch.Tensor, out: torch.Tensor,
+                shared: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        S = 0 if shared is None else shared.shape[1]
+        cap = y.numel() // self.H
+        ep_combine(self.h, y, cap, topk_weights, shared, S, out, stream)
+        return out
+
+    def expert_identity(self, quant: int, recv_data, recv_scales, y, mark_mod: int = 0,
+                        stream=None) -> torch.Tensor:
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        cap = min(recv_data.numel() // db, y.numel() // self.H)
+        ep_expert_identity(self.h, quant, recv_data, recv_scales, cap, mark_mod, y, stream)
+        return y

@@ -1,0 +1,239 @@
+/*
+ * ep_layout.h -- C ABI of the GB300 (sm_103a) MoE expert-parallel token
+ * layout, dispatch and combine library (libeplayout.so).
+ *
+ * One GPU holds all R logical expert-parallel ranks.  Rank j owns the E/R
+ * experts [j*L, (j+1)*L) (L = E/R local experts, no shared-expert ranks), and
+ * its receive buffer is the slice of rows [rank_base[j], rank_base[j+1]) of
+ * one device allocation.  The "all-to-all" of the pages is the dispatch
+ * kernel's scatter into those slices; nothing crosses a GPU boundary.
+ *
+ * The operations follow three pages:
+ *   - DeepEP "Normal Mode API" (sgl-kernel-npu NORMAL_API.md): Buffer.dispatch
+ *     layout inputs (num_tokens_per_rank, is_token_in_rank,
+ *     num_tokens_per_expert, topk_idx with -1 = no expert, expert_alignment),
+ *     its returns (recv_x formats, num_recv_tokens_per_expert_list, the handle
+ *     that "must be passed unchanged to combine"), and Buffer.combine
+ *     ("multiply by weights and sum").
+ *   - CANN "aclnnMoeDistributeDispatchV2": the Formula section (quantMode 0,
+ *     2 and 4), the two-phase workspace-query-then-execute convention with a
+ *     status code, deterministic computing, and localExpertNum =
+ *     moeExpertNum / epWorldSize.
+ *   - Modular MAX "max.nn.comm.ep.EPBatchManager": ep_dispatch outputs
+ *     (expert_start_indices, expert_ids, expert_usage_stats, src_info) and
+ *     ep_combine (weighted sum of routed expert outputs, plus the fused
+ *     shared-expert outputs).
+ *
+ * Conventions for every entry point:
+ *   - All arrays are caller-owned.  Device arrays are plain device pointers;
+ *     the library never allocates device memory.  Host arrays are noted.
+ *   - Launching calls are asynchronous and ordered on the given stream (a
+ *     cudaStream_t; NULL is the legacy default stream).  Only the calls marked
+ *     "synchronises" wait for the stream.
+ *   - Invalid arguments are rejected on the host, before any launch, with
+ *     EP_ERR_INVALID_ARG or EP_ERR_UNSUPPORTED and no side effects.
+ *   - Errors found on the device (a bad expert id, a capacity overflow) are
+ *     recorded in a sticky status word of the handle; read it with
+ *     ep_handle_status().  A CUDA launch error returns EP_ERR_CUDA.
+ *   - Results are bit-for-bit deterministic: no slot is assigned by an atomic.
+ *   - Layouts are row-major.  bf16 tensors are passed as raw 16-bit storage.
+ */
+#ifndef EP_LAYOUT_H
+#define EP_LAYOUT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* ep_stream_t;
+
+/* Status codes (the aclnn convention of returning a status from every call). */
+typedef enum ep_status {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,   /* an argument violates a documented constraint */
+    EP_ERR_UNSUPPORTED = 2,   /* a valid combination this build does not implement */
+    EP_ERR_CAPACITY = 3,      /* the layout needs more receive rows than provided */
+    EP_ERR_BAD_EXPERT_ID = 4, /* a topk id outside [-1, E); the entry was treated as -1 */
+    EP_ERR_TIMEOUT = 5,       /* reserved: no kernel of this build waits on another */
+    EP_ERR_CUDA = 6           /* a CUDA runtime call or kernel launch failed */
+} ep_status;
+
+/* Receive-row encodings (CANN quantMode numbering for 0 and 2; the MX variants
+ * of quantMode 4 are split by element type). */
+typedef enum ep_quant_mode {
+    EP_QUANT_NONE = 0,           /* bf16 rows [rows, H] (quantMode 0) */
+    EP_QUANT_INT8_PER_TOKEN = 2, /* int8 [rows, H] + float32 inverse scale [rows] (quantMode 2) */
+    EP_QUANT_MXFP8_E4M3 = 4,     /* e4m3 [rows, H] + e8m0 [rows, H/32] (quantMode 4) */
+    EP_QUANT_MXFP8_E5M2 = 5,     /* e5m2 [rows, H] + e8m0 [rows, H/32] (quantMode 4) */
+    EP_QUANT_MXFP4_E2M1 = 6      /* e2m1 x2 [rows, H/2] + e8m0 [rows, H/32] */
+} ep_quant_mode;
+
+/* Problem description.  Constraints (checked by ep_params_validate):
+ *   num_ranks R >= 1; num_experts E in [1, 512] with E % R == 0 (localExpertNum
+ *   = moeExpertNum / epWorldSize); topk K in [1, min(16, E)]; tokens_per_rank
+ *   T in [0, 65536] (T = 0 is legal and routes nothing); hidden H in [8, 8192]
+ *   with H % 8 == 0 (16-byte rows; MX modes need H % 32 == 0);
+ *   expert_alignment alpha in [1, 4096]; recv_capacity_rows >= 0 (0 = the
+ *   worst case R*T*K + E*(alpha-1), which can never overflow). */
+typedef struct ep_params {
+    int32_t num_ranks;          /* R: logical EP ranks on this GPU */
+    int32_t tokens_per_rank;    /* T: source tokens per rank */
+    int32_t hidden;             /* H: hidden size (elements per token row) */
+    int32_t num_experts;        /* E: routed experts, L = E/R per rank */
+    int32_t topk;               /* K: experts per token */
+    int32_t expert_alignment;   /* alpha: per-expert row count granularity */
+    int64_t recv_capacity_rows; /* rows of recv_src kept in the workspace */
+} ep_params;
+
+/* Opaque handle: host-side bookkeeping plus device arrays carved out of the
+ * caller's workspace.  It holds every index and prefix matrix combine needs
+ * (the DeepEP handle that "must be passed unchanged to combine"). */
+typedef struct ep_handle ep_handle;
+
+/* Device views of the layout a handle holds (all inside the workspace).
+ * Shapes: cnt [R,E] (num_tokens_per_expert of each source rank);
+ * is_token_in_rank [R,T,R] (0/1 bytes); num_tokens_per_rank [R,R];
+ * recv_cnt [E]; aligned_cnt [E] = [R,L] (num_recv_tokens_per_expert_list,
+ * aligned); expert_start [R,L+1] (expert_start_indices of each rank, rows
+ * relative to the rank); rank_base [R+1] (first global row of each rank,
+ * rank_base[R] = total rows); expert_base [E+1] (first global row of each
+ * expert); src_prefix [R,E] (entries that earlier source ranks send to e);
+ * dst_row [R,T,K] (receive row of each entry, -1 = no expert); recv_src
+ * [recv_src_capacity] (source token s*T+t of each row, -1 on padding: MAX's
+ * src_info); expert_ids [R,L]; expert_usage_stats [R,2] = [max aligned count
+ * over the rank's experts, experts with at least one token]. */
+typedef struct ep_layout_views {
+    const int32_t* cnt;
+    const uint8_t* is_token_in_rank;
+    const int32_t* num_tokens_per_rank;
+    const int32_t* recv_cnt;
+    const int32_t* aligned_cnt;
+    const int32_t* expert_start;
+    const int64_t* rank_base;
+    const int32_t* expert_base;
+    const int32_t* src_prefix;
+    const int32_t* dst_row;
+    const int32_t* recv_src;
+    const int32_t* expert_ids;
+    const int32_t* expert_usage_stats;
+    int64_t recv_src_capacity;
+} ep_layout_views;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* ep_status_string(ep_status status);
+
+/* Host only.  Checks the constraints listed at ep_params. */
+ep_status ep_params_validate(const ep_params* params);
+
+/* Host only.  Device workspace bytes that ep_handle_create needs for params
+ * (the first phase of the aclnn two-phase call).  Writes *bytes. */
+ep_status ep_layout_workspace_size(const ep_params* params, size_t* bytes);
+
+/* Host only.  Bytes of one receive row's data part and scale part for a quant
+ * mode and hidden size (bf16: 2H and 0; int8: H and 4; e4m3/e5m2: H and H/32;
+ * e2m1: H/2 and H/32).  H must satisfy the mode's divisibility rule. */
+ep_status ep_recv_row_bytes(int32_t hidden, ep_quant_mode quant,
+                            int64_t* data_bytes, int64_t* scale_bytes);
+
+/* Host only.  Builds a handle over a caller-owned device workspace of at least
+ * ep_layout_workspace_size() bytes, 256-byte aligned.  The small host-side
+ * struct is allocated with malloc; free it with ep_handle_destroy.  The
+ * workspace must outlive the handle.  A handle can be reused for many
+ * ep_layout calls with the same params. */
+ep_status ep_handle_create(const ep_params* params, void* workspace,
+                           size_t workspace_bytes, ep_handle** out);
+
+/* Host only.  Frees the host-side struct (not the workspace).  NULL is a no-op. */
+ep_status ep_handle_destroy(ep_handle* handle);
+
+/* Device.  The routing layout (DeepEP layout inputs, CANN expert placement,
+ * MAX expert_start_indices) from topk_idx [R,T,K] int64 (device), where -1
+ * means no expert: per-(source rank, expert) counts, is_token_in_rank,
+ * num_tokens_per_rank, aligned per-expert counts, per-rank expert starts and
+ * rank bases, source-rank prefixes, dst_row and recv_src.  Receive rows are
+ * grouped by destination rank, then local expert; inside an expert segment
+ * they follow (source rank, token, slot) ascending, and alpha-padding rows
+ * sit at the segment's end.  Resets the handle's status word first.  Ids
+ * outside [-1, E) set EP_ERR_BAD_EXPERT_ID and count as -1; more rows than
+ * recv_capacity_rows sets EP_ERR_CAPACITY (recv_src then holds only the rows
+ * that fit).  Three kernels, no host synchronisation. */
+ep_status ep_layout(ep_handle* handle, const int64_t* topk_idx, ep_stream_t stream);
+
+/* Host only.  Device pointers to the layout arrays (valid after ep_layout's
+ * kernels have run on the stream). */
+ep_status ep_handle_views(const ep_handle* handle, ep_layout_views* out);
+
+/* Synchronises the stream, then copies rank_base [R+1] (int64) to host memory:
+ * the receive rows of rank j are rank_base[j+1] - rank_base[j]. */
+ep_status ep_handle_recv_rows(const ep_handle* handle, int64_t* rank_base_host,
+                              ep_stream_t stream);
+
+/* Synchronises the stream, then copies the aligned per-local-expert receive
+ * counts [R*L] (int32) to host memory: DeepEP's
+ * num_recv_tokens_per_expert_list, one list per rank. */
+ep_status ep_handle_expert_counts(const ep_handle* handle, int32_t* aligned_host,
+                                  ep_stream_t stream);
+
+/* Synchronises the stream and returns the sticky device status word (EP_OK,
+ * EP_ERR_CAPACITY or EP_ERR_BAD_EXPERT_ID), or EP_ERR_CUDA. */
+ep_status ep_handle_status(const ep_handle* handle, ep_stream_t stream);
+
+/* Device.  Dispatch (CANN Formula, quantMode 0 / 2 / 4; DeepEP recv_x): every
+ * valid entry (s,t,k) receives token (s,t)'s row of x [R*T, H] bf16 (device)
+ * at receive row dst_row[s,t,k], encoded per quant:
+ *   NONE: the bf16 row, bit for bit;
+ *   INT8_PER_TOKEN: s = 127/max|x| (IEEE division), code = round-half-even
+ *     (x*s) clamped to [-127,127], scale word = 1/s (float32; 0 for an
+ *     all-zero row);
+ *   MXFP8/MXFP4: per 32-element block, sharedExp = floor(log2(max|x|)) - emax
+ *     clamped to [-127,127] (-127 when the max is zero or subnormal), code =
+ *     cast(x / 2^sharedExp) rounded to nearest even and saturated to the
+ *     largest finite value, scale byte = sharedExp + 127 (e8m0, the decode
+ *     scale); e2m1 packs element 2i in the low nibble of byte i.
+ * Each row is read once and quantised once, then written to its K rows.
+ * Padding rows get all-zero data and scale bytes.  recv_data holds
+ * recv_rows_capacity rows of ep_recv_row_bytes().data_bytes; recv_scales
+ * holds as many rows of scale_bytes (NULL for NONE).  If the layout needs more
+ * rows than recv_rows_capacity, nothing is written and the status word gets
+ * EP_ERR_CAPACITY.  x, recv_data and recv_scales must be 16-byte aligned
+ * (recv_scales 4-byte aligned suffices). */
+ep_status ep_dispatch(const ep_handle* handle, const void* x, ep_quant_mode quant,
+                      void* recv_data, void* recv_scales, int64_t recv_rows_capacity,
+                      ep_stream_t stream);
+
+/* Device.  Combine (DeepEP combine, MAX ep_combine): for every source token,
+ *   out[s,t,:] = bf16( sum_k w[s,t,k] * y[dst_row[s,t,k],:]
+ *                      + sum_{q<num_shared} shared[s,q,t,:] )
+ * accumulated in float32 (k in order, then q), rounded once to bf16 (nearest
+ * even).  Entries with dst_row = -1 are skipped; a token without experts gets
+ * the shared sum (or zeros).  y [y_rows_capacity, H] bf16 holds the expert
+ * outputs in receive layout (device); topk_weights [R,T,K] float32 (device);
+ * shared [R, num_shared, T, H] bf16 (device, NULL when num_shared = 0); out
+ * [R*T, H] bf16 (device).  If the layout has more rows than y_rows_capacity,
+ * nothing is written and the status word gets EP_ERR_CAPACITY.  Pointers to
+ * bf16 data must be 16-byte aligned. */
+ep_status ep_combine(const ep_handle* handle, const void* y, int64_t y_rows_capacity,
+                     const float* topk_weights, const void* shared, int32_t num_shared,
+                     void* out, ep_stream_t stream);
+
+/* Device.  Stand-in expert for tests and benchmarks (not part of dispatch or
+ * combine): y[r,:] = bf16(dequant(recv row r) * 2^-(e(r) mod mark_mod)), where
+ * e(r) is the row's expert, dequant is the bf16 value (NONE), q * scale
+ * (INT8_PER_TOKEN) or code value * 2^sharedExp (MX), and mark_mod = 0 means
+ * no mark.  Padding rows give zeros.  Shapes as in ep_dispatch; y is
+ * [rows_capacity, H] bf16. */
+ep_status ep_expert_identity(const ep_handle* handle, ep_quant_mode quant,
+                             const void* recv_data, const void* recv_scales,
+                             int64_t rows_capacity, int32_t mark_mod, void* y,
+                             ep_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_LAYOUT_H */

@@ -9,6 +9,11 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
+    # compile the CUDA library (cross-compiles without a GPU) and the oracle
+    from combine_ep_layout_03_gb300 import build as _build
+    import oracle as _oracle
+    _build.build()
+    _oracle.build()
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: full-size workloads")
 

@@ -1,0 +1,164 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/ep_layout.h declares, and rejects invalid arguments on the host before
+any CUDA call (the aclnn convention of validating in the first phase)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from combine_ep_layout_03_gb300 import ep
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep_layout.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    names = set(re.findall(r"\b(ep_[a-z_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("ep_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_size",
+                 "ep_handle_create", "ep_handle_destroy", "ep_handle_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", ep.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert getattr(ep.lib, n) is not None
+
+
+def good():
+    return ep.make_params(8, 4096, 7168, 256, 8, 1, 0)
+
+
+@pytest.mark.parametrize("field,value", [
+    ("num_ranks", 0), ("num_experts", 0), ("num_experts", 513), ("num_experts", 250),
+    ("topk", 0), ("topk", 17), ("tokens_per_rank", -1), ("tokens_per_rank", 65537),
+    ("hidden", 0), ("hidden", 7164), ("hidden", 8200), ("expert_alignment", 0),
+    ("recv_capacity_rows", -5)])
+def test_validation_rejects(field, value):
+    p = good()
+    setattr(p, field, value)
+    assert ep.ep_params_validate(p) == ep.EP_ERR_INVALID_ARG
+    with pytest.raises(ep.EPError) as ei:
+        ep.ep_layout_workspace_size(p)
+    assert ei.value.status == ep.EP_ERR_INVALID_ARG
+
+
+def test_topk_larger_than_experts_rejected():
+    p = ep.make_params(2, 8, 64, 4, 5, 1, 0)
+    assert ep.ep_params_validate(p) == ep.EP_ERR_INVALID_ARG
+
+
+def test_validation_accepts_the_workloads():
+    from combine_ep_layout_03_gb300 import synth
+    for w in synth.WORKLOADS.values():
+        p = ep.make_params(w.R, w.T, w.H, w.E, w.K, w.alpha, 0)
+        assert ep.ep_params_validate(p) == ep.EP_OK
+    assert ep.ep_params_validate(ep.make_params(4, 0, 1024, 16, 2, 1, 0)) == ep.EP_OK  # T = 0
+
+
+def test_row_bytes():
+    assert ep.ep_recv_row_bytes(7168, ep.EP_QUANT_NONE) == (14336, 0)
+    assert ep.ep_recv_row_bytes(7168, ep.EP_QUANT_INT8_PER_TOKEN) == (7168, 4)
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_MXFP8_E4M3) == (4096, 128)
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_MXFP8_E5M2) == (4096, 128)
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_MXFP4_E2M1) == (2048, 128)
+    with pytest.raises(ep.EPError):
+        ep.ep_recv_row_bytes(4104, ep.EP_QUANT_MXFP8_E4M3)  # H % 32 != 0 for MX
+    with pytest.raises(ep.EPError) as ei:
+        ep.ep_recv_row_bytes(4096, 3)
+    assert ei.value.status == ep.EP_ERR_UNSUPPORTED
+
+
+def _create_fake(p, base=1 << 40):
+    """Handle over a fake, never dereferenced device address (host-only calls)."""
+    n = ep.ep_layout_workspace_size(p)
+    h = ctypes.c_void_p(0)
+    st = ep.lib.ep_handle_create(ctypes.byref(p), base, n, ctypes.byref(h))
+    return st, h.value, n
+
+
+def test_workspace_carving_is_aligned_and_disjoint():
+    from combine_ep_layout_03_gb300.ep import _VIEW_SPECS
+    for w in (ep.make_params(8, 4096, 7168, 256, 8, 1, 0), ep.make_params(32, 8192, 4096, 512, 16, 64, 0),
+              ep.make_params(3, 0, 64, 6, 2, 4, 0), ep.make_params(2, 5, 16, 2, 2, 3, 100)):
+        st, h, n = _create_fake(w)
+        assert st == ep.EP_OK
+        v = ep.ep_handle_views(h)
+        R, T, E, K = w.num_ranks, w.tokens_per_rank, w.num_experts, w.topk
+
+        class S:
+            pass
+        s = S()
+        s.R, s.T, s.E, s.K, s.L = R, T, E, K, E // R
+        s.recv_src_capacity = v.recv_src_capacity
+        worst = R * T * K + E * (w.expert_alignment - 1)
+        assert v.recv_src_capacity == (w.recv_capacity_rows or worst)
+        spans = []
+        for name, (dt, shape) in _VIEW_SPECS.items():
+            ptr = getattr(v, name)
+            size = 1
+            for d in shape(s):
+                size *= d
+            nbytes = size * {1: 1, 4: 4, 8: 8}[{"torch.uint8": 1, "torch.int32": 4, "torch.int64": 8}[str(dt)]]
+            assert (ptr - (1 << 40)) % 256 == 0, name
+            spans.append((ptr, ptr + nbytes, name))
+        spans.sort()
+        for (a0, a1, na), (b0, b1, nb) in zip(spans, spans[1:]):
+            assert a1 <= b0, (na, nb)
+        assert spans[-1][1] <= (1 << 40) + n
+        ep.ep_handle_destroy(h)
+
+
+def test_create_rejects_bad_workspace():
+    p = good()
+    n = ep.ep_layout_workspace_size(p)
+    h = ctypes.c_void_p(0)
+    assert ep.lib.ep_handle_create(ctypes.byref(p), (1 << 40) + 8, n, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_handle_create(ctypes.byref(p), 1 << 40, n - 1, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_handle_create(ctypes.byref(p), None, n, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+
+
+def test_launching_calls_validate_before_touching_cuda():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    assert st == ep.EP_OK
+    L = ep.lib
+    # unsupported quant mode, unaligned pointers, negative capacities
+    assert L.ep_dispatch(h, 1 << 40, 3, 1 << 41, None, 10, None) == ep.EP_ERR_UNSUPPORTED
+    assert L.ep_dispatch(h, (1 << 40) + 2, 0, 1 << 41, None, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(h, 1 << 40, 2, 1 << 41, None, 10, None) == ep.EP_ERR_INVALID_ARG  # no scales
+    assert L.ep_dispatch(h, 1 << 40, 0, 1 << 41, None, -1, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_combine(h, 1 << 40, 10, None, None, 0, 1 << 41, None) == ep.EP_ERR_INVALID_ARG  # no weights
+    assert L.ep_combine(h, 1 << 40, 10, 1 << 42, None, 2, 1 << 41, None) == ep.EP_ERR_INVALID_ARG  # no shared
+    assert L.ep_combine(h, 1 << 40, 10, 1 << 42, None, 0, (1 << 41) + 4, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_layout(h, None, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_expert_identity(h, 9, 1 << 40, None, 4, 0, 1 << 41, None) == ep.EP_ERR_UNSUPPORTED
+    assert L.ep_expert_identity(h, 0, 1 << 40, None, 4, -1, 1 << 41, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_layout(None, None, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
+    # MX dispatch on a hidden size that is not a multiple of 32
+    p = ep.make_params(2, 8, 40, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    assert L.ep_dispatch(h, 1 << 40, 4, 1 << 41, 1 << 42, 10, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
+
+
+def test_status_strings():
+    for code, name in [(0, "EP_OK"), (1, "EP_ERR_INVALID_ARG"), (3, "EP_ERR_CAPACITY"),
+                       (4, "EP_ERR_BAD_EXPERT_ID"), (6, "EP_ERR_CUDA")]:
+        assert ep.status_string(code) == name

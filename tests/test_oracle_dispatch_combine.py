@@ -202,3 +202,24 @@ def test_expert_dequant_rows(q):
         tol = {oracle.Q_INT8: 1 / 127, oracle.Q_E4M3: 2 ** -3, oracle.Q_E2M1: 0.5}[q]
         amax = np.max(np.abs(src))
         assert np.max(np.abs(y[i] - src)) <= tol * amax * 1.01
+
+
+@pytest.mark.parametrize("idx,q", [(5, oracle.Q_NONE), (3, oracle.Q_INT8), (4, oracle.Q_E2M1)])
+def test_sampled_combine_matches_full_oracle(idx, q):
+    # the GPU tests' one-token-at-a-time oracle path equals the whole-buffer path
+    from gpu_harness import oracle_combine_sampled
+    w = small(idx, 12)
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    x = synth.gen_x(w)
+    shared = synth.gen_shared(w)
+    lay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    data, scales = oracle.dispatch(lay, x, q)
+    y = oracle.expert_rows(lay, np.arange(lay.rows), w.H, q, data, scales, 8)
+    full = oracle.combine(lay, y, wts, shared)
+    tokens = np.array([0, 3, w.N - 1, w.N // 2])
+    sh_tok = None
+    if shared is not None:
+        sh_tok = shared.transpose(0, 2, 1, 3).reshape(w.N, w.num_shared, w.H)[tokens]
+    o, ref, mag = oracle_combine_sampled(lay, x.reshape(w.N, w.H), wts, sh_tok, q, 8, tokens)
+    assert np.array_equal(o, full[tokens])
