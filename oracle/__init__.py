@@ -315,13 +315,13 @@ def combine_within_tolerance(got_bits: np.ndarray, ref: np.ndarray, mag: np.ndar
     """Combine tolerance, derived from the arithmetic (fp32 accumulation, one bf16
     rounding at the end):
       every element: |got - ref| <= 2 ulp_bf16(ref) + (2K+S+1) 2^-24 sum|terms|;
-      elements with |ref| >= 2^-10 sum|terms| (no heavy cancellation):
+      elements with ref != 0 and |ref| >= 2^-10 sum|terms| (no heavy cancellation):
       max |got - ref| / |ref| <= 1e-2.
     ref is the float64 sum.  Returns (ok, max_abs_excess, max_rel)."""
     got = bf16_bits_to_f64(got_bits)
     err = np.abs(got - ref)
     bound = 2.0 * ulp_bf16(ref) + combine_tolerance_floor(mag, K, S)
     excess = float(np.max(err - bound)) if err.size else 0.0
-    sel = np.abs(ref) >= np.ldexp(mag, -10)
+    sel = (np.abs(ref) >= np.ldexp(mag, -10)) & (ref != 0)
     rel = float(np.max(err[sel] / np.abs(ref[sel]))) if np.any(sel) else 0.0
     return bool(excess <= 0.0 and rel <= 1e-2), excess, rel
