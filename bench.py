@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work")
+    p.add_argument("--tokens-per-rank", type=int, default=0,
+                   help="override T (small cases for profiling; not a bench line)")
     return p.parse_args(argv)
 
 
@@ -300,16 +302,18 @@ def run_ours(args, w, quant, rank, local_rank, world):
 
 # --------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, quant, topk, wts, x_bits, sh0_bits, budget_s):
+def oracle_sample(w, quant, topk, wts, x_bits, sh_bits, budget_s):
     """The oracle as it stands, single-threaded: layout over the whole routing,
     then dispatch (rows one by one through recv_src) and combine of the first n
-    source tokens of rank 0, n chosen so the work takes about budget_s.
-    Returns (tokens/s, description, seconds spent)."""
+    source tokens, n chosen so the work takes about budget_s.  sh_bits holds the
+    shared rows of the leading ranks ([R', S, T, H]) or None.
+    Returns (tokens/s, description, seconds spent, n)."""
     import oracle
     t0 = time.perf_counter()
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
     t_layout = time.perf_counter() - t0
     K = w.K
+    n_max = w.N if sh_bits is None else sh_bits.shape[0] * w.T
 
     def run(n):
         tokens = np.arange(n)
@@ -325,21 +329,20 @@ def oracle_sample(w, quant, topk, wts, x_bits, sh0_bits, budget_s):
         else:
             y = oracle.expert_rows(olay, rows, w.H, quant, data, scales)
         c = time.perf_counter()
-        sh = None if sh0_bits is None else sh0_bits
-        oracle.combine(olay, y, wts, sh, 0, n, ymap)
+        oracle.combine(olay, y, wts, sh_bits, 0, n, ymap)
         dd = time.perf_counter()
         return (b - a) + (dd - c)
 
-    n = min(w.T, 8)
+    n = min(n_max, 8)
     t = run(n)
     spent = t_layout + t
-    while t < budget_s * 0.5 and n < w.T:
-        n = int(min(w.T, max(n * 2, n * budget_s / max(t, 1e-3))))
+    while t < budget_s * 0.5 and n < n_max:
+        n = int(min(n_max, max(n * 2, n * budget_s / max(t, 1e-3))))
         t = run(n)
         spent += t
     per_token = t_layout / w.N + t / n
     desc = (f"layout of all {w.N} tokens ({t_layout*1e3:.1f} ms) + dispatch and combine of the "
-            f"first {n} tokens of rank 0 ({t:.2f} s), extrapolated per token")
+            f"first {n} source tokens ({t:.2f} s), extrapolated per token")
     return 1.0 / per_token, desc, spent, n
 
 
@@ -347,10 +350,10 @@ def host_x_bits(x_dev, w):
     return x_dev.contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.N, w.H)
 
 
-def host_shared0(sh_dev, w):
+def host_shared_lead(sh_dev, w, ranks=2):
     if sh_dev is None:
         return None
-    return sh_dev[0:1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return sh_dev[0:ranks].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 # --------------------------------------------------------------------- main
@@ -372,6 +375,8 @@ def main(argv=None):
     from combine_ep_layout_03_gb300 import synth
     idx, quant = WORKLOAD_KEYS[args.workload]
     w = synth.WORKLOADS[idx]
+    if args.tokens_per_rank:
+        w = w.with_(T=args.tokens_per_rank)
 
     if args.impl == "reference":
         if rank != 0:
@@ -408,7 +413,7 @@ def main(argv=None):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xb = host_x_bits(res["x_dev"], w)
-        sh0 = host_shared0(res["sh_dev"], w)
+        sh0 = host_shared_lead(res["sh_dev"], w)
         v, desc, spent, n = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget)
         cpu = {"value": round(v, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": desc}
@@ -452,7 +457,7 @@ def run_reference(args, w, quant):
     topk = synth.gen_topk(w)
     wts = synth.gen_weights(w, topk)
     x_bits = synth.gen_x(w).reshape(w.N, w.H)
-    sh = synth.gen_shared(w.with_(R=1)) if w.num_shared else None
+    sh = synth.gen_shared(w.with_(R=2)) if w.num_shared else None
     budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
     vals, descs = [], None
     for i in range(args.warmup + args.steps):
