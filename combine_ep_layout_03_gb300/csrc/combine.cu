@@ -3,15 +3,19 @@
 // sum"; MAX EPBatchManager.ep_combine: weighted sum of routed expert outputs,
 // plus the fused shared-expert outputs), rounded once to bf16.
 //
-// One CTA per token at a time (grid-stride, persistent grid).  Warp 0 compacts
-// the token's valid slots (ballot) into shared memory in slot order, so the
-// gather loop has no per-slot branch.  Each thread owns VPT 16-byte vectors of
-// the row (vector index u * NT + tid: contiguous 512-byte runs per warp) and
-// accumulates 8 * VPT floats with FMA.
+// Persistent grid, one CTA per SM, tokens round-robin over CTAs.  Warp 0 is a
+// producer: per token it compacts the valid slots (ballot, slot order kept),
+// and per chunk of the row it bulk-loads (cp.async.bulk, TMA) the chunk of each
+// valid expert row and of each shared row into a shared-memory stage, tracked
+// by the stage's "full" mbarrier.  The consumer warps accumulate the chunk in
+// float32 (FMA, slot order, then the shared rows), round to bf16 and store,
+// then release the stage on its "empty" mbarrier.  No register staging, so
+// the bytes in flight are bounded only by the stage ring.
 //
 // The stand-in expert (ep_expert_identity) is also here: it dequantises
 // receive rows back to bf16 for tests and benchmarks.
 #include "ep_internal.cuh"
+#include "tma.cuh"
 
 namespace {
 
@@ -39,83 +43,135 @@ __device__ __forceinline__ void acc_add(float acc[8], const uint4& v) {
     acc[7] += __uint_as_float(v.w & 0xffff0000u);
 }
 
-template <int VPT>
-__global__ void __launch_bounds__(256)
-combine_kernel(CombineArgs a) {
-    __shared__ int sdst[kMaxTopk];
-    __shared__ float sw[kMaxTopk];
-    __shared__ int skv;
+// Stage ring of the bulk-copy combine.  A work item is one chunk of CH
+// elements of one token's output row; a stage holds the chunk of each of the
+// token's valid expert rows (slot order) followed by its S shared rows, plus
+// the compacted weights.
+struct CombineTma {
+    int CH;          // elements per chunk (multiple of 8)
+    int nch;         // chunks per row
+    int rows;        // K + S row slots per stage
+    int stage_bytes; // rows * CH * 2, rounded up to 128
+    int nstages;
+    int nconsumer;   // consumer threads (multiple of 32)
+};
+
+constexpr int kMetaInts = 32;   // per stage: [0] = valid slots, [1..16] = weights
+
+__global__ void __launch_bounds__(288)
+combine_tma_kernel(CombineArgs a, CombineTma c) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    int32_t* meta = reinterpret_cast<int32_t*>(smem + (size_t)c.nstages * c.stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(meta + c.nstages * kMetaInts);
+    uint64_t* empty = full + c.nstages;
     const int total = a.expert_base[a.E];
     if ((int64_t)total > a.cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
         return;
     }
-    const int NT = blockDim.x;
-    const int tid = threadIdx.x, lane = tid & 31;
-    for (int64_t n = blockIdx.x; n < a.N; n += gridDim.x) {
-        __syncthreads();
-        if (tid < 32) {
-            int d = -1;
-            float wt = 0.0f;
-            if (lane < a.K) {
-                d = a.dst_row[n * a.K + lane];
-                wt = a.w[n * a.K + lane];
-            }
-            const unsigned mask = __ballot_sync(kFull, d >= 0);
-            if (d >= 0) {
-                const int p = __popc(mask & ((1u << lane) - 1u));
-                sdst[p] = d;
-                sw[p] = wt;
-            }
-            if (lane == 0) skv = __popc(mask);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ncw = c.nconsumer >> 5;
+    if (tid == 0) {
+        for (int s = 0; s < c.nstages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], ncw);
         }
-        __syncthreads();
-        const int kv = skv;
-        float acc[VPT][8];
-#pragma unroll
-        for (int u = 0; u < VPT; ++u)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-        for (int k = 0; k < kv; ++k) {
-            const uint16_t* yrow = a.y + (int64_t)sdst[k] * a.H;
-            const float wt = sw[k];
-            uint4 v[VPT];
-#pragma unroll
-            for (int u = 0; u < VPT; ++u) {
-                const int vi = u * NT + tid;
-                v[u] = vi < a.nvec ? ld_nc_v4(yrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < VPT; ++u) acc_fma(acc[u], v[u], wt);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int64_t G = gridDim.x;
+    const int64_t cnt = a.N > (int64_t)blockIdx.x ? (a.N - 1 - blockIdx.x) / G + 1 : 0;
+    const int rowb = c.CH * 2;
+
+    if (warp == 0) {
+        // producer: lane k < K holds slot k of the current token (next one prefetched)
+        int dn = -1;
+        float wn = 0.0f;
+        if (cnt > 0 && lane < a.K) {
+            const int64_t n = blockIdx.x;
+            dn = a.dst_row[n * a.K + lane];
+            wn = a.w[n * a.K + lane];
         }
-        if (a.S > 0) {
-            const int64_t s = n / a.T, t = n - (n / a.T) * a.T;
-            for (int q = 0; q < a.S; ++q) {
-                const uint16_t* srow = a.shared + ((s * a.S + q) * a.T + t) * a.H;
-                uint4 v[VPT];
-#pragma unroll
-                for (int u = 0; u < VPT; ++u) {
-                    const int vi = u * NT + tid;
-                    v[u] = vi < a.nvec ? ld_nc_v4(srow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0);
+        bool ok = true;
+        for (int64_t j = 0; j < cnt && ok; ++j) {
+            const int64_t n = blockIdx.x + j * G;
+            const int d = dn;
+            const float wt = wn;
+            if (j + 1 < cnt && lane < a.K) {
+                const int64_t nn = n + G;
+                dn = a.dst_row[nn * a.K + lane];
+                wn = a.w[nn * a.K + lane];
+            }
+            const unsigned mask = __ballot_sync(0xffffffffu, d >= 0);
+            const int kv = __popc(mask);
+            const int p = __popc(mask & ((1u << lane) - 1u));
+            const int64_t sr = n / a.T, tt = n - (n / a.T) * a.T;
+            for (int ci = 0; ci < c.nch; ++ci) {
+                const int64_t q = j * c.nch + ci;
+                const int s = (int)(q % c.nstages);
+                const int64_t u = q / c.nstages;
+                if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), kMaxPolls)) ok = false;
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                const int e0 = ci * c.CH;
+                const int ce = min(c.CH, a.H - e0);
+                const uint32_t cb = (uint32_t)ce * 2;
+                int32_t* m = meta + s * kMetaInts;
+                for (int k = 0; k < a.K; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, wt, k);
+                    const int pk = __shfl_sync(0xffffffffu, p, k);
+                    if (lane == 0 && ((mask >> k) & 1u)) m[1 + pk] = __float_as_int(wk);
                 }
-#pragma unroll
-                for (int u = 0; u < VPT; ++u) acc_add(acc[u], v[u]);
+                if (lane == 0) {
+                    m[0] = kv;
+                    mbar_arrive_expect_tx(&full[s], cb * (uint32_t)(kv + a.S));
+                }
+                __syncwarp();
+                uint8_t* st = stages + (size_t)s * c.stage_bytes;
+                if (d >= 0) bulk_load(st + (size_t)p * rowb, a.y + (int64_t)d * a.H + e0, cb, &full[s]);
+                if (lane < a.S)
+                    bulk_load(st + (size_t)(kv + lane) * rowb,
+                              a.shared + ((sr * a.S + lane) * a.T + tt) * a.H + e0, cb, &full[s]);
             }
         }
-        uint16_t* orow = a.out + n * a.H;
+        if (!ok && lane == 0) ep_set_status(a.status, EP_ERR_TIMEOUT);
+        return;
+    }
+
+    // consumers: vector v of the chunk, v = ct + i * nconsumer
+    const int ct = tid - 32;
+    bool ok = true;
+    for (int64_t j = 0; j < cnt && ok; ++j) {
+        const int64_t n = blockIdx.x + j * G;
+        for (int ci = 0; ci < c.nch; ++ci) {
+            const int64_t q = j * c.nch + ci;
+            const int s = (int)(q % c.nstages);
+            if (!mbar_wait(&full[s], (uint32_t)((q / c.nstages) & 1), kMaxPolls)) { ok = false; break; }
+            const int32_t* m = meta + s * kMetaInts;
+            const int kv = m[0];
+            const int e0 = ci * c.CH;
+            const int nv = min(c.CH, a.H - e0) >> 3;
+            const uint8_t* st = stages + (size_t)s * c.stage_bytes;
+            for (int v = ct; v < nv; v += c.nconsumer) {
+                float acc[8];
 #pragma unroll
-        for (int u = 0; u < VPT; ++u) {
-            const int vi = u * NT + tid;
-            if (vi < a.nvec) {
+                for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                for (int r = 0; r < kv; ++r)
+                    acc_fma(acc, lds_v4(st + (size_t)r * rowb + v * 16), __int_as_float(m[1 + r]));
+                for (int qq = 0; qq < a.S; ++qq)
+                    acc_add(acc, lds_v4(st + (size_t)(kv + qq) * rowb + v * 16));
                 uint4 o;
-                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
-                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
-                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
-                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
-                st_v4(orow + (int64_t)vi * 8, o);
+                o.x = pack_bf16x2_rn(acc[0], acc[1]);
+                o.y = pack_bf16x2_rn(acc[2], acc[3]);
+                o.z = pack_bf16x2_rn(acc[4], acc[5]);
+                o.w = pack_bf16x2_rn(acc[6], acc[7]);
+                st_v4(a.out + n * a.H + e0 + v * 8, o);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
     }
+    if (!ok && lane == 0) ep_set_status(a.status, EP_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- identity expert
@@ -190,14 +246,31 @@ identity_kernel(IdentityArgs a) {
 
 cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st) {
     if (a.N == 0) return cudaSuccess;
-    constexpr int VPT = 4;
-    const int nt = ((a.nvec + VPT - 1) / VPT + 31) / 32 * 32;
-    int occ = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, combine_kernel<VPT>, nt, 0);
+    CombineTma c;
+    c.rows = a.K + a.S;
+    // ~32 KB of row chunks per stage, chunks of equal size (multiples of 8 elements)
+    int ch = (16384 / c.rows) & ~7;
+    if (ch < 8) ch = 8;
+    if (ch > a.H) ch = a.H;
+    int nch = (a.H + ch - 1) / ch;
+    ch = ((a.H + nch - 1) / nch + 7) & ~7;
+    nch = (a.H + ch - 1) / ch;
+    c.CH = ch;
+    c.nch = nch;
+    c.stage_bytes = (c.rows * ch * 2 + 127) / 128 * 128;
+    const int per_stage = c.stage_bytes + kMetaInts * 4 + 16;
+    c.nstages = kCombineSmemBudget / per_stage;
+    if (c.nstages > 16) c.nstages = 16;
+    if (c.nstages < 2) return cudaErrorInvalidConfiguration;
+    c.nconsumer = ((ch / 8 + 31) / 32) * 32;
+    if (c.nconsumer > 256) c.nconsumer = 256;
+    const size_t smem = (size_t)c.nstages * per_stage;
+    cudaError_t err = cudaFuncSetAttribute(combine_tma_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
+    int64_t grid = h->num_sms;
     if (grid > a.N) grid = a.N;
-    combine_kernel<VPT><<<(unsigned)grid, nt, 0, st>>>(a);
+    combine_tma_kernel<<<(unsigned)grid, 32 + c.nconsumer, smem, st>>>(a, c);
     return cudaGetLastError();
 }
 

@@ -13,7 +13,17 @@
 // is read once, encoded once, then written to its K destination rows.  Work
 // items past the last token zero the alpha-padding rows, one expert each.
 // The four lanes 4m..4m+3 hold one 32-element MX block at the same u.
+//
+// bf16 rows (quantMode 0) take a register-free path instead: one thread per
+// CTA drives the bulk-copy (TMA) engine.  A ring of shared-memory stages holds
+// a source row plus the 16-byte-aligned window of its dst_row entries, both
+// loaded by cp.async.bulk onto the stage's mbarrier; the row is then written
+// to its K destination rows by cp.async.bulk stores, one bulk group per token,
+// and a stage is refilled once cp.async.bulk.wait_group.read shows the stores
+// issued kTmaLag tokens earlier have read it.  Warps 1..3 of the CTA zero the
+// padding rows meanwhile.
 #include "ep_internal.cuh"
+#include "tma.cuh"
 
 namespace {
 
@@ -219,6 +229,107 @@ dispatch_kernel(DispatchArgs a) {
     }
 }
 
+constexpr int kTmaLag = 4;          // bulk-store groups allowed to read a stage
+constexpr int kDstSlotInts = 32;    // 128-byte slot per stage for the dst_row window
+
+__device__ void zero_rows_part(const DispatchArgs& a, int64_t r0, int64_t r1, int part, int nparts) {
+    if (r1 <= r0) return;
+    const int64_t nbytes = (r1 - r0) * a.row_bytes;
+    uint8_t* base = a.data + r0 * a.row_bytes;
+    for (int64_t i = part; i < nbytes / 16; i += nparts) st_v4(base + i * 16, make_uint4(0, 0, 0, 0));
+}
+
+__global__ void __launch_bounds__(128)
+dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    int32_t* sdst = reinterpret_cast<int32_t*>(smem + (size_t)nstages * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)nstages * (stage_bytes + kDstSlotInts * 4));
+    const int total = a.expert_base[a.E];
+    if ((int64_t)total > a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
+        return;
+    }
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < nstages; ++s) mbar_init(&full[s], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid >= 32) {
+        // padding rows (alpha > 1): one expert per CTA at a time
+        for (int e = blockIdx.x; e < a.E; e += gridDim.x) {
+            const int64_t r0 = (int64_t)a.expert_base[e] + a.recv_cnt[e];
+            zero_rows_part(a, r0, a.expert_base[e + 1], tid - 32, blockDim.x - 32);
+        }
+        return;
+    }
+    if (tid != 0) return;
+
+    const int64_t G = gridDim.x;
+    const int64_t cnt = a.N > (int64_t)blockIdx.x ? (a.N - 1 - blockIdx.x) / G + 1 : 0;
+    const uint32_t row = (uint32_t)a.row_bytes;
+    const uint8_t* dst_bytes = reinterpret_cast<const uint8_t*>(a.dst_row);
+    auto issue = [&](int64_t j) {
+        const int s = (int)(j % nstages);
+        const int64_t n = blockIdx.x + j * G;
+        const int64_t first = n * a.K;
+        const int64_t b0 = (first * 4) & ~(int64_t)15;
+        const int64_t b1 = ((first + a.K) * 4 + 15) & ~(int64_t)15;
+        const uint32_t wbytes = (uint32_t)(b1 - b0);
+        mbar_arrive_expect_tx(&full[s], row + wbytes);
+        bulk_load(stages + (size_t)s * stage_bytes, a.x + n * a.H, row, &full[s]);
+        bulk_load(sdst + s * kDstSlotInts, dst_bytes + b0, wbytes, &full[s]);
+    };
+    const int64_t pro = cnt < nstages ? cnt : nstages;
+    for (int64_t j = 0; j < pro; ++j) issue(j);
+    bool ok = true;
+    int64_t j = 0;
+    for (; j < cnt; ++j) {
+        const int s = (int)(j % nstages);
+        if (!mbar_wait(&full[s], (uint32_t)((j / nstages) & 1), kMaxPolls)) { ok = false; break; }
+        const int64_t n = blockIdx.x + j * G;
+        const int32_t* d = sdst + s * kDstSlotInts + (int)((n * a.K) & 3);
+        const uint8_t* src = stages + (size_t)s * stage_bytes;
+        for (int k = 0; k < a.K; ++k) {
+            const int r = d[k];
+            if (r >= 0) bulk_store(a.data + (int64_t)r * row, src, row);
+        }
+        bulk_commit();
+        if (j >= kTmaLag) {
+            bulk_wait_read<kTmaLag>();
+            const int64_t t = j - kTmaLag + nstages;
+            if (t < cnt) issue(t);
+        }
+    }
+    bulk_wait_all();
+    if (!ok) {
+        ep_set_status(a.status, EP_ERR_TIMEOUT);
+        // let every load already issued land before the CTA's shared memory is released
+        const int64_t issued = (j >= kTmaLag ? j - kTmaLag + nstages : pro);
+        for (int64_t i = j; i < issued && i < cnt; ++i)
+            mbar_wait(&full[i % nstages], (uint32_t)((i / nstages) & 1), kMaxPolls);
+    }
+}
+
+cudaError_t launch_bf16_tma(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
+    const int stage_bytes = (a.row_bytes + 127) / 128 * 128;
+    const int per_stage = stage_bytes + kDstSlotInts * 4 + 8;
+    int nstages = kDispatchSmemBudget / per_stage;
+    if (nstages > 32) nstages = 32;
+    if (nstages < kTmaLag + 2) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)nstages * per_stage;
+    cudaError_t err = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int64_t grid = h->num_sms;
+    const int64_t items = a.N > a.E ? a.N : a.E;
+    if (grid > items) grid = items;
+    if (grid < 1) grid = 1;
+    dispatch_bf16_tma_kernel<<<(unsigned)grid, 128, smem, st>>>(a, nstages, stage_bytes);
+    return cudaGetLastError();
+}
+
 template <int Q>
 cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     constexpr int VPT = 4;
@@ -238,7 +349,7 @@ cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st)
 
 cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
     switch (quant) {
-        case M_NONE: return launch_q<M_NONE>(h, a, st);
+        case M_NONE: return launch_bf16_tma(h, a, st);
         case M_INT8: return launch_q<M_INT8>(h, a, st);
         case M_E4M3: return launch_q<M_E4M3>(h, a, st);
         case M_E5M2: return launch_q<M_E5M2>(h, a, st);

@@ -275,7 +275,7 @@ ep_status ep_combine(const ep_handle* hc, const void* y, int64_t y_cap, const fl
                      const void* shared, int32_t S, void* out, ep_stream_t stream) {
     ep_handle* h = const_cast<ep_handle*>(hc);
     if (!h) return EP_ERR_INVALID_ARG;
-    if (S < 0 || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
+    if (S < 0 || S > kMaxShared || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
     if (y_cap < 0) return EP_ERR_INVALID_ARG;
     if (h->N > 0) {
         if (!w || !aligned_to(w, 4) || !out || !aligned_to(out, 16)) return EP_ERR_INVALID_ARG;

@@ -13,6 +13,9 @@ constexpr int kLayoutThreads = 256;
 constexpr int kLayoutTargetBlocks = 608;  // 4 x 152 SMs; fixes the workspace size
 constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 512;
+constexpr int kMaxShared = 16;     // shared-expert rows per token in combine
+constexpr int kDispatchSmemBudget = 200 * 1024;  // shared-memory ring of the bulk-copy kernels
+constexpr int kCombineSmemBudget = 200 * 1024;
 
 struct ep_handle {
     ep_params p;

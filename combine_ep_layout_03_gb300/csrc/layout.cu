@@ -109,14 +109,15 @@ layout_scan_kernel(LayoutArgs a) {
             a.cnt[(int64_t)s * a.E + e] = next - a.src_prefix[(int64_t)s * a.E + e];
         }
     }
-    // num_tokens_per_rank[s][j] = sum over the rank's CTAs
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t gsz = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t g = gid; g < (int64_t)a.R * a.R; g += gsz) {
+    // num_tokens_per_rank[s][j] = sum over the rank's CTAs, one warp per (s, j)
+    const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g = gwarp; g < (int64_t)a.R * a.R; g += nwarps) {
         const int s = (int)(g / a.R), j = (int)(g - (int64_t)s * a.R);
         int acc = 0;
-        for (int c = 0; c < a.C; ++c) acc += a.blk_rank[((int64_t)s * a.C + c) * a.R + j];
-        a.ntpr[g] = acc;
+        for (int c = tx; c < a.C; c += 32) acc += a.blk_rank[((int64_t)s * a.C + c) * a.R + j];
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (tx == 0) a.ntpr[g] = acc;
     }
 }
 

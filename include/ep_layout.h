@@ -59,7 +59,7 @@ typedef enum ep_status {
     EP_ERR_UNSUPPORTED = 2,   /* a valid combination this build does not implement */
     EP_ERR_CAPACITY = 3,      /* the layout needs more receive rows than provided */
     EP_ERR_BAD_EXPERT_ID = 4, /* a topk id outside [-1, E); the entry was treated as -1 */
-    EP_ERR_TIMEOUT = 5,       /* reserved: no kernel of this build waits on another */
+    EP_ERR_TIMEOUT = 5,       /* a bounded wait inside a kernel (on a bulk copy's mbarrier) gave up */
     EP_ERR_CUDA = 6           /* a CUDA runtime call or kernel launch failed */
 } ep_status;
 
@@ -213,7 +213,8 @@ ep_status ep_dispatch(const ep_handle* handle, const void* x, ep_quant_mode quan
  * even).  Entries with dst_row = -1 are skipped; a token without experts gets
  * the shared sum (or zeros).  y [y_rows_capacity, H] bf16 holds the expert
  * outputs in receive layout (device); topk_weights [R,T,K] float32 (device);
- * shared [R, num_shared, T, H] bf16 (device, NULL when num_shared = 0); out
+ * shared [R, num_shared, T, H] bf16 (device, NULL when num_shared = 0;
+ * num_shared in [0, 16]); out
  * [R*T, H] bf16 (device).  If the layout has more rows than y_rows_capacity,
  * nothing is written and the status word gets EP_ERR_CAPACITY.  Pointers to
  * bf16 data must be 16-byte aligned. */

@@ -162,3 +162,10 @@ def test_status_strings():
     for code, name in [(0, "EP_OK"), (1, "EP_ERR_INVALID_ARG"), (3, "EP_ERR_CAPACITY"),
                        (4, "EP_ERR_BAD_EXPERT_ID"), (6, "EP_ERR_CUDA")]:
         assert ep.status_string(code) == name
+
+
+def test_combine_rejects_too_many_shared_rows():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    assert ep.lib.ep_combine(h, 1 << 40, 10, 1 << 42, 1 << 43, 17, 1 << 41, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
