@@ -48,6 +48,13 @@ class ep_layout_views(ctypes.Structure):
         "expert_ids", "expert_usage_stats")] + [("recv_src_capacity", ctypes.c_int64)]
 
 
+class ep_layout_outputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "status", "cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt", "aligned_cnt",
+        "expert_start", "rank_base", "expert_base", "src_prefix", "dst_row", "recv_src",
+        "expert_ids", "expert_usage_stats")]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libeplayout.so is not built ({LIB_PATH}); run "
@@ -70,6 +77,7 @@ def _load():
         "ep_dispatch": ([vp, vp, st, vp, vp, i64, vp], st),
         "ep_combine": ([vp, vp, i64, vp, vp, i32, vp, vp], st),
         "ep_expert_identity": ([vp, st, vp, vp, i64, i32, vp, vp], st),
+        "ep_layout_static_scratch": ([P, vp, ctypes.POINTER(ep_layout_outputs), vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -290,3 +298,11 @@ class EPLayout:
         cap = min(recv_data.numel() // db, y.numel() // self.H)
         ep_expert_identity(self.h, quant, recv_data, recv_scales, cap, mark_mod, y, stream)
         return y
+
+
+def ep_layout_static_scratch(p: ep_params, topk_idx, outputs: dict, stream=None) -> None:
+    """The layout without any device allocation: ``outputs`` maps each field of
+    ep_layout_outputs to a caller-owned device tensor (or pointer)."""
+    o = ep_layout_outputs(**{k: _ptr(outputs[k]) for k, _ in ep_layout_outputs._fields_})
+    _check(_lib.ep_layout_static_scratch(ctypes.byref(p), _ptr(topk_idx), ctypes.byref(o),
+                                         _stream(stream)), "ep_layout_static_scratch")

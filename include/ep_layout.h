@@ -233,6 +233,43 @@ ep_status ep_expert_identity(const ep_handle* handle, ep_quant_mode quant,
                              int64_t rows_capacity, int32_t mark_mod, void* y,
                              ep_stream_t stream);
 
+/* Writable device arrays of one layout, for ep_layout_static_scratch.  Shapes
+ * as in ep_layout_views; status is one int32 word (the sticky status word). */
+typedef struct ep_layout_outputs {
+    int32_t* status;
+    int32_t* cnt;
+    uint8_t* is_token_in_rank;
+    int32_t* num_tokens_per_rank;
+    int32_t* recv_cnt;
+    int32_t* aligned_cnt;
+    int32_t* expert_start;
+    int64_t* rank_base;
+    int32_t* expert_base;
+    int32_t* src_prefix;
+    int32_t* dst_row;
+    int32_t* recv_src;          /* recv_capacity_rows entries (0: the worst case) */
+    int32_t* expert_ids;
+    int32_t* expert_usage_stats;
+} ep_layout_outputs;
+
+/* Device.  The same layout as ep_layout, for callers that cannot allocate
+ * device memory (an operator running where the host framework forbids device
+ * allocation, a serving loop that allocates only at start-up, a C host without
+ * a device allocator).  The pages have no counterpart to this entry point.
+ *
+ * The caller passes topk_idx and every output array; the call allocates
+ * nothing.  The layout's scratch (per-CTA histograms) lives in a fixed 2 MiB
+ * device array owned by the library, present on every GPU that loads it until
+ * the process exits.  Problems whose scratch exceeds 2 MiB (about 608 CTAs x
+ * (E + R) x 4 bytes) return EP_ERR_UNSUPPORTED before any launch.  All calls
+ * share the array: calls whose kernels may overlap on the GPU race and must be
+ * serialised by the caller.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  Status values as for ep_layout,
+ * written to outputs->status. */
+ep_status ep_layout_static_scratch(const ep_params* params, const int64_t* topk_idx,
+                                   const ep_layout_outputs* outputs, ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
