@@ -39,16 +39,22 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
+    """Compile and link.  ``defines`` (e.g. ["EP_COMBINE_GROUPS=2"]) override
+    compile-time tunables; ``out`` names another output file (variants)."""
+    lib = out or LIB
+    if not force and not defines and out is None and up_to_date():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
+    objdir = os.path.join(OUT_DIR, "obj_" + os.path.basename(lib).replace(".so", ""))
+    os.makedirs(objdir, exist_ok=True)
+    dflags = [f"-D{d}" for d in defines]
     cc = nvcc()
     inc = ["-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, *inc, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *dflags, *inc, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -60,16 +66,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, log in results:
             sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(os.path.join(OUT_DIR, "ptxas.log"), "w") as f:
+    os.replace(tmp, lib)
+    with open(os.path.join(objdir, "ptxas.log"), "w") as f:
         for _, log in results:
             f.write(log)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -53,12 +53,25 @@ struct CombineTma {
     int rows;        // K + S row slots per stage
     int stage_bytes; // rows * CH * 2, rounded up to 128
     int nstages;
-    int nconsumer;   // consumer threads (multiple of 32)
+    int nconsumer;   // consumer threads per group (multiple of 32)
+    int ngroups;     // consumer groups; group g reduces items q = g (mod ngroups)
 };
 
 constexpr int kMetaInts = 32;   // per stage: [0] = valid slots, [1..16] = weights
 
-__global__ void __launch_bounds__(288)
+// Tunables (compile-time): target bytes of row chunks per stage, and the
+// number of consumer groups that reduce different work items concurrently.
+#ifndef EP_COMBINE_STAGE_TARGET
+#define EP_COMBINE_STAGE_TARGET 98304
+#endif
+#ifndef EP_COMBINE_GROUPS
+#define EP_COMBINE_GROUPS 1
+#endif
+#ifndef EP_COMBINE_MAX_THREADS
+#define EP_COMBINE_MAX_THREADS 512
+#endif
+
+__global__ void __launch_bounds__(32 + EP_COMBINE_MAX_THREADS)
 combine_tma_kernel(CombineArgs a, CombineTma c) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
@@ -71,7 +84,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
         return;
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ncw = c.nconsumer >> 5;
+    const int ncw = c.nconsumer >> 5;   // warps of one consumer group
     if (tid == 0) {
         for (int s = 0; s < c.nstages; ++s) {
             mbar_init(&full[s], 1);
@@ -138,38 +151,42 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
         return;
     }
 
-    // consumers: vector v of the chunk, v = ct + i * nconsumer
-    const int ct = tid - 32;
+    // consumers: group g takes items q = g (mod ngroups); vector v of the
+    // chunk is handled by thread ct + i * nconsumer of the group
+    const int g = (tid - 32) / c.nconsumer;
+    const int ct = (tid - 32) - g * c.nconsumer;
+    const int64_t items = cnt * c.nch;
     bool ok = true;
-    for (int64_t j = 0; j < cnt && ok; ++j) {
+    for (int64_t q = g; q < items; q += c.ngroups) {
+        const int64_t j = q / c.nch;
+        const int ci = (int)(q - j * c.nch);
         const int64_t n = blockIdx.x + j * G;
-        for (int ci = 0; ci < c.nch; ++ci) {
-            const int64_t q = j * c.nch + ci;
-            const int s = (int)(q % c.nstages);
-            if (!mbar_wait(&full[s], (uint32_t)((q / c.nstages) & 1), kMaxPolls)) { ok = false; break; }
-            const int32_t* m = meta + s * kMetaInts;
-            const int kv = m[0];
-            const int e0 = ci * c.CH;
-            const int nv = min(c.CH, a.H - e0) >> 3;
-            const uint8_t* st = stages + (size_t)s * c.stage_bytes;
-            for (int v = ct; v < nv; v += c.nconsumer) {
-                float acc[8];
+        const int s = (int)(q % c.nstages);
+        if (!mbar_wait(&full[s], (uint32_t)((q / c.nstages) & 1), kMaxPolls)) { ok = false; break; }
+        const int32_t* m = meta + s * kMetaInts;
+        const int kv = m[0];
+        const int e0 = ci * c.CH;
+        const int nv = min(c.CH, a.H - e0) >> 3;
+        const uint8_t* st = stages + (size_t)s * c.stage_bytes;
+        for (int v = ct; v < nv; v += c.nconsumer) {
+            float acc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-                for (int r = 0; r < kv; ++r)
-                    acc_fma(acc, lds_v4(st + (size_t)r * rowb + v * 16), __int_as_float(m[1 + r]));
-                for (int qq = 0; qq < a.S; ++qq)
-                    acc_add(acc, lds_v4(st + (size_t)(kv + qq) * rowb + v * 16));
-                uint4 o;
-                o.x = pack_bf16x2_rn(acc[0], acc[1]);
-                o.y = pack_bf16x2_rn(acc[2], acc[3]);
-                o.z = pack_bf16x2_rn(acc[4], acc[5]);
-                o.w = pack_bf16x2_rn(acc[6], acc[7]);
-                st_v4(a.out + n * a.H + e0 + v * 8, o);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            const uint8_t* col = st + v * 16;
+#pragma unroll 4
+            for (int r = 0; r < kv; ++r)
+                acc_fma(acc, lds_v4(col + (size_t)r * rowb), __int_as_float(m[1 + r]));
+            for (int qq = 0; qq < a.S; ++qq)
+                acc_add(acc, lds_v4(col + (size_t)(kv + qq) * rowb));
+            uint4 o;
+            o.x = pack_bf16x2_rn(acc[0], acc[1]);
+            o.y = pack_bf16x2_rn(acc[2], acc[3]);
+            o.z = pack_bf16x2_rn(acc[4], acc[5]);
+            o.w = pack_bf16x2_rn(acc[6], acc[7]);
+            st_v4(a.out + n * a.H + e0 + v * 8, o);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
     if (!ok && lane == 0) ep_set_status(a.status, EP_ERR_TIMEOUT);
 }
@@ -248,8 +265,9 @@ cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_
     if (a.N == 0) return cudaSuccess;
     CombineTma c;
     c.rows = a.K + a.S;
-    // ~32 KB of row chunks per stage, chunks of equal size (multiples of 8 elements)
-    int ch = (16384 / c.rows) & ~7;
+    // about EP_COMBINE_STAGE_TARGET bytes of row chunks per stage, chunks of
+    // equal size (multiples of 8 elements)
+    int ch = (EP_COMBINE_STAGE_TARGET / 2 / c.rows) & ~7;
     if (ch < 8) ch = 8;
     if (ch > a.H) ch = a.H;
     int nch = (a.H + ch - 1) / ch;
@@ -264,13 +282,22 @@ cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_
     if (c.nstages < 2) return cudaErrorInvalidConfiguration;
     c.nconsumer = ((ch / 8 + 31) / 32) * 32;
     if (c.nconsumer > 256) c.nconsumer = 256;
+    c.ngroups = EP_COMBINE_GROUPS;
+    while (c.ngroups > 1 && c.ngroups * c.nconsumer > EP_COMBINE_MAX_THREADS) --c.ngroups;
+    if (c.ngroups > c.nstages) c.ngroups = c.nstages;
+    if (c.ngroups < 1) c.ngroups = 1;
+    // Every use of a stage must belong to the same consumer group: item q and
+    // item q + nstages share a stage, so nstages is a multiple of ngroups.  A
+    // group then waits on a stage's uses in order and is never more than one
+    // phase ahead of its "full" barrier (phase-parity waits cannot alias).
+    c.nstages = c.nstages / c.ngroups * c.ngroups;
     const size_t smem = (size_t)c.nstages * per_stage;
     cudaError_t err = cudaFuncSetAttribute(combine_tma_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     int64_t grid = h->num_sms;
     if (grid > a.N) grid = a.N;
-    combine_tma_kernel<<<(unsigned)grid, 32 + c.nconsumer, smem, st>>>(a, c);
+    combine_tma_kernel<<<(unsigned)grid, 32 + c.ngroups * c.nconsumer, smem, st>>>(a, c);
     return cudaGetLastError();
 }
 

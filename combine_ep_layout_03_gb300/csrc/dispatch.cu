@@ -7,12 +7,14 @@
 //                code = cast(x / 2^sharedExp) (e4m3 / e5m2, and e2m1 packed x2),
 //                e8m0 scale byte sharedExp + 127.
 //
-// One CTA handles one token at a time (grid-stride, persistent grid).  Each
-// thread holds VPT 16-byte vectors of the row in registers at vector index
-// u * NT + tid, so every warp access is one contiguous 512-byte run.  The row
-// is read once, encoded once, then written to its K destination rows.  Work
-// items past the last token zero the alpha-padding rows, one expert each.
-// The four lanes 4m..4m+3 hold one 32-element MX block at the same u.
+// Quantised rows: one CTA handles one token at a time (grid-stride, persistent
+// grid).  Each thread holds VPT 16-byte vectors of the row in registers at
+// vector index u * NT + tid, so every warp access is one contiguous 512-byte
+// run.  The row is read once and encoded once in registers; the encoded row
+// is staged in shared memory and written to its K destination rows by bulk
+// (TMA) stores.  Work items past the last token zero the alpha-padding rows,
+// one expert each.  The four lanes 4m..4m+3 hold one 32-element MX block at
+// the same u.
 //
 // bf16 rows (quantMode 0) take a register-free path instead: one thread per
 // CTA drives the bulk-copy (TMA) engine.  A ring of shared-memory stages holds
@@ -104,9 +106,16 @@ __device__ void zero_rows(const DispatchArgs& a, int64_t r0, int64_t r1) {
     }
 }
 
-template <int Q, int VPT>
+// Quantised rows.  BULK: the encoded row (and, for MX rows whose scale row is
+// a multiple of 16 bytes, the scale row) is written once into one of two
+// shared-memory stages and thread 0 sends it to the K destination rows with
+// cp.async.bulk stores (one bulk group per token; a stage is rewritten only
+// after wait_group.read shows the group of two tokens earlier has read it).
+// Otherwise every thread stores its codes to each destination itself.
+template <int Q, int VPT, bool BULK>
 __global__ void __launch_bounds__(256)
-dispatch_kernel(DispatchArgs a) {
+dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) {
+    extern __shared__ __align__(128) uint8_t qstage[];
     __shared__ int sdst[kMaxTopk];
     __shared__ uint32_t sred[8];
     const int total = a.expert_base[a.E];
@@ -117,6 +126,7 @@ dispatch_kernel(DispatchArgs a) {
     const int NT = blockDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t items = a.N + a.E;
+    int64_t j = 0;  // tokens handled by this CTA so far
     for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
         if (w >= a.N) {
             const int e = (int)(w - a.N);
@@ -125,7 +135,10 @@ dispatch_kernel(DispatchArgs a) {
             zero_rows(a, r0, r1);
             continue;
         }
-        __syncthreads();  // sdst / sred of the previous token are consumed
+        if constexpr (BULK) {
+            if (tid == 0 && j >= 2) bulk_wait_read<1>();
+        }
+        __syncthreads();  // sdst / sred / the stage of two tokens ago are free
         if (tid < a.K) sdst[tid] = a.dst_row[w * a.K + tid];
         const uint16_t* xrow = a.x + w * a.H;
         uint4 v[VPT];
@@ -143,51 +156,31 @@ dispatch_kernel(DispatchArgs a) {
         }
         __syncthreads();
 
-        if constexpr (Q == M_NONE) {
-            for (int k = 0; k < a.K; ++k) {
-                const int d = sdst[k];
-                if (d < 0) continue;
-                uint8_t* row = a.data + (int64_t)d * a.row_bytes;
-#pragma unroll
-                for (int u = 0; u < VPT; ++u) {
-                    const int vi = u * NT + tid;
-                    if (vi < a.nvec) st_v4(row + (int64_t)vi * 16, v[u]);
-                }
-            }
-        } else if constexpr (Q == M_INT8) {
+        // encode: code words per vector (8 bytes for int8 / fp8, 4 for e2m1)
+        uint32_t packed[VPT][2];
+        uint32_t sbyte[VPT];
+        float inv = 0.0f;
+        if constexpr (Q == M_INT8) {
             uint32_t m = 0;
             for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i]);
             const float amax = bf16_bits_to_float(m);
             const float s = __fdiv_rn(127.0f, amax);      // +inf for an all-zero row
-            const float inv = __fdiv_rn(1.0f, s);          // 0 for an all-zero row
-            uint2 code[VPT];
+            inv = __fdiv_rn(1.0f, s);                      // 0 for an all-zero row
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
                 float f[8];
                 unpack8(v[u], f);
+                sbyte[u] = 0;
                 if (amax > 0.0f) {
-                    code[u].x = q8(f[0], s) | (q8(f[1], s) << 8) | (q8(f[2], s) << 16) | (q8(f[3], s) << 24);
-                    code[u].y = q8(f[4], s) | (q8(f[5], s) << 8) | (q8(f[6], s) << 16) | (q8(f[7], s) << 24);
+                    packed[u][0] = q8(f[0], s) | (q8(f[1], s) << 8) | (q8(f[2], s) << 16) | (q8(f[3], s) << 24);
+                    packed[u][1] = q8(f[4], s) | (q8(f[5], s) << 8) | (q8(f[6], s) << 16) | (q8(f[7], s) << 24);
                 } else {
-                    code[u] = make_uint2(0, 0);
+                    packed[u][0] = packed[u][1] = 0;
                 }
-            }
-            for (int k = 0; k < a.K; ++k) {
-                const int d = sdst[k];
-                if (d < 0) continue;
-                uint8_t* row = a.data + (int64_t)d * a.row_bytes;
-#pragma unroll
-                for (int u = 0; u < VPT; ++u) {
-                    const int vi = u * NT + tid;
-                    if (vi < a.nvec) st_v2(row + (int64_t)vi * 8, code[u]);
-                }
-                if (tid == 0) reinterpret_cast<float*>(a.scales)[d] = inv;
             }
         } else {
             // MX: block b = vi / 4 lives in lanes 4m..4m+3 at the same u
             constexpr int emax = MxTraits<Q>::emax;
-            uint32_t packed[VPT][2];
-            uint32_t sbyte[VPT];
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
                 uint32_t m = vec_absmax_bits(v[u]);
@@ -210,26 +203,75 @@ dispatch_kernel(DispatchArgs a) {
                     packed[u][1] = cvt_fp8x2<Q>(f[4], f[5]) | (cvt_fp8x2<Q>(f[6], f[7]) << 16);
                 }
             }
-            for (int k = 0; k < a.K; ++k) {
-                const int d = sdst[k];
-                if (d < 0) continue;
+        }
+        constexpr int VB = (Q == M_E2M1) ? 4 : 8;  // code bytes per 16-byte source vector
+
+        if constexpr (BULK) {
+            uint8_t* stg = qstage + (size_t)(j & 1) * stage_bytes;
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                const int vi = u * NT + tid;
+                if (vi < a.nvec) {
+                    if constexpr (VB == 4) *reinterpret_cast<uint32_t*>(stg + vi * 4) = packed[u][0];
+                    else *reinterpret_cast<uint2*>(stg + vi * 8) = make_uint2(packed[u][0], packed[u][1]);
+                    if (Q != M_INT8 && scale_bulk && (vi & 3) == 0) stg[scale_off + (vi >> 2)] = (uint8_t)sbyte[u];
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                for (int k = 0; k < a.K; ++k) {
+                    const int d = sdst[k];
+                    if (d < 0) continue;
+                    bulk_store(a.data + (int64_t)d * a.row_bytes, stg, (uint32_t)a.row_bytes);
+                    if (Q != M_INT8 && scale_bulk)
+                        bulk_store(a.scales + (int64_t)d * a.scale_bytes, stg + scale_off,
+                                   (uint32_t)a.scale_bytes);
+                }
+                bulk_commit();
+            }
+        }
+        for (int k = 0; k < a.K; ++k) {
+            const int d = sdst[k];
+            if (d < 0) continue;
+            if constexpr (Q == M_INT8) {
+                if (tid == 0) reinterpret_cast<float*>(a.scales)[d] = inv;
+            } else {
+                if (!(BULK && scale_bulk)) {
+                    uint8_t* srow = a.scales + (int64_t)d * a.scale_bytes;
+#pragma unroll
+                    for (int u = 0; u < VPT; ++u) {
+                        const int vi = u * NT + tid;
+                        if (vi < a.nvec && (vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
+                    }
+                }
+            }
+            if constexpr (!BULK) {
                 uint8_t* row = a.data + (int64_t)d * a.row_bytes;
-                uint8_t* srow = a.scales + (int64_t)d * a.scale_bytes;
 #pragma unroll
                 for (int u = 0; u < VPT; ++u) {
                     const int vi = u * NT + tid;
                     if (vi < a.nvec) {
-                        if constexpr (Q == M_E2M1) st_u32(row + (int64_t)vi * 4, packed[u][0]);
+                        if constexpr (VB == 4) st_u32(row + (int64_t)vi * 4, packed[u][0]);
                         else st_v2(row + (int64_t)vi * 8, make_uint2(packed[u][0], packed[u][1]));
-                        if ((vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
                     }
                 }
             }
         }
+        ++j;
+    }
+    if constexpr (BULK) {
+        if (tid == 0) bulk_wait_all();
     }
 }
 
-constexpr int kTmaLag = 4;          // bulk-store groups allowed to read a stage
+#ifndef EP_DISPATCH_LAG
+#define EP_DISPATCH_LAG 4
+#endif
+#ifndef EP_DISPATCH_CTAS_PER_SM
+#define EP_DISPATCH_CTAS_PER_SM 1
+#endif
+constexpr int kTmaLag = EP_DISPATCH_LAG;  // bulk-store groups allowed to read a stage
 constexpr int kDstSlotInts = 32;    // 128-byte slot per stage for the dst_row window
 
 __device__ void zero_rows_part(const DispatchArgs& a, int64_t r0, int64_t r1, int part, int nparts) {
@@ -315,14 +357,14 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
 cudaError_t launch_bf16_tma(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     const int stage_bytes = (a.row_bytes + 127) / 128 * 128;
     const int per_stage = stage_bytes + kDstSlotInts * 4 + 8;
-    int nstages = kDispatchSmemBudget / per_stage;
+    int nstages = kDispatchSmemBudget / EP_DISPATCH_CTAS_PER_SM / per_stage;
     if (nstages > 32) nstages = 32;
     if (nstages < kTmaLag + 2) return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)nstages * per_stage;
     cudaError_t err = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    int64_t grid = h->num_sms;
+    int64_t grid = (int64_t)h->num_sms * EP_DISPATCH_CTAS_PER_SM;
     const int64_t items = a.N > a.E ? a.N : a.E;
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
@@ -330,19 +372,36 @@ cudaError_t launch_bf16_tma(const ep_handle* h, const DispatchArgs& a, cudaStrea
     return cudaGetLastError();
 }
 
-template <int Q>
-cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
+template <int Q, bool BULK>
+cudaError_t launch_q_impl(const ep_handle* h, const DispatchArgs& a, int nt, int stage_bytes,
+                          int scale_off, int scale_bulk, cudaStream_t st) {
     constexpr int VPT = 4;
-    const int nt = ((a.nvec + VPT - 1) / VPT + 31) / 32 * 32;
+    const size_t smem = BULK ? 2 * (size_t)stage_bytes : 0;
     int occ = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dispatch_kernel<Q, VPT>, nt, 0);
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dispatch_kernel<Q, VPT, BULK>,
+                                                                    nt, smem);
     if (err != cudaSuccess) return err;
     const int64_t items = a.N + a.E;
     int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
-    dispatch_kernel<Q, VPT><<<(unsigned)grid, nt, 0, st>>>(a);
+    dispatch_kernel<Q, VPT, BULK><<<(unsigned)grid, nt, smem, st>>>(a, stage_bytes, scale_off, scale_bulk);
     return cudaGetLastError();
+}
+
+template <int Q>
+cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
+    constexpr int VPT = 4;
+    const int nt = ((a.nvec + VPT - 1) / VPT + 31) / 32 * 32;
+    // bulk stores need 16-byte rows (the receive buffer itself is 16-byte aligned)
+    const bool bulk = (a.row_bytes % 16) == 0;
+    if (!bulk) return launch_q_impl<Q, false>(h, a, nt, 0, 0, 0, st);
+    const int scale_bulk = (Q != M_INT8 && a.scale_bytes % 16 == 0 &&
+                            ((uintptr_t)a.scales % 16) == 0) ? 1 : 0;
+    const int scale_off = (a.row_bytes + 15) / 16 * 16;
+    int stage_bytes = scale_off + (scale_bulk ? (a.scale_bytes + 15) / 16 * 16 : 0);
+    stage_bytes = (stage_bytes + 127) / 128 * 128;
+    return launch_q_impl<Q, true>(h, a, nt, stage_bytes, scale_off, scale_bulk, st);
 }
 
 }  // namespace

@@ -15,7 +15,10 @@ constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxShared = 16;     // shared-expert rows per token in combine
 constexpr int kDispatchSmemBudget = 200 * 1024;  // shared-memory ring of the bulk-copy kernels
-constexpr int kCombineSmemBudget = 200 * 1024;
+#ifndef EP_COMBINE_SMEM_BUDGET
+#define EP_COMBINE_SMEM_BUDGET (200 * 1024)
+#endif
+constexpr int kCombineSmemBudget = EP_COMBINE_SMEM_BUDGET;
 
 struct ep_handle {
     ep_params p;
@@ -31,7 +34,7 @@ struct ep_handle {
     int num_sms;        // 0 until the first launch queries it
     // device arrays inside the workspace
     int32_t* status;
-    int32_t* blk_hist;      // [B][E] per-CTA expert counts, then per-CTA exclusive prefixes
+    int32_t* blk_hist;      // [E][B] per-CTA expert counts, then per-CTA exclusive prefixes
     int32_t* blk_rank;      // [B][R] per-CTA tokens per destination rank
     int32_t* cnt;           // [R][E]
     uint8_t* itr;           // [N][R]

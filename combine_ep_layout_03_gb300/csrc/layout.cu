@@ -6,9 +6,11 @@
 //   count  - per CTA (a contiguous token range of one source rank): expert
 //            histogram in shared memory, is_token_in_rank (one warp per token),
 //            tokens per destination rank.
-//   scan   - per expert column: exclusive prefix of the CTA histograms over
-//            CTAs (global order = source rank, then token), per-source-rank
-//            counts and prefixes, received totals; num_tokens_per_rank.
+//   scan   - one CTA per expert: exclusive prefix of that expert's column of
+//            CTA histograms (stored expert-major, so the column is contiguous)
+//            over CTAs (global order = source rank, then token), per-source-
+//            rank counts and prefixes, received totals; further CTAs sum
+//            num_tokens_per_rank, one warp per (source, destination) pair.
 //   assign - per CTA: exclusive scan of the aligned counts (expert bases),
 //            then a warp-ordered pass: __match_any_sync ranks equal experts
 //            inside each 32-entry step, per-warp running counters keep the
@@ -65,60 +67,8 @@ layout_count_kernel(LayoutArgs a) {
     }
     if (bad) ep_set_status(a.status, EP_ERR_BAD_EXPERT_ID);
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.blk_hist[(int64_t)b * a.E + e] = hist[e];
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.blk_hist[(int64_t)e * a.B + b] = hist[e];
     for (int j = threadIdx.x; j < a.R; j += blockDim.x) a.blk_rank[(int64_t)b * a.R + j] = rcnt[j];
-}
-
-// 32 expert columns per CTA; 32 row slices of the CTA-histogram matrix each.
-__global__ void __launch_bounds__(1024)
-layout_scan_kernel(LayoutArgs a) {
-    __shared__ int part[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int e = blockIdx.x * 32 + tx;
-    const int per = (a.B + 31) / 32;
-    const int b0 = min(a.B, ty * per), b1 = min(a.B, b0 + per);
-    int sum = 0;
-    if (e < a.E)
-        for (int b = b0; b < b1; ++b) sum += a.blk_hist[(int64_t)b * a.E + e];
-    part[ty][tx] = sum;
-    __syncthreads();
-    if (ty == 0) {
-        int run = 0;
-        for (int i = 0; i < 32; ++i) {
-            const int v = part[i][tx];
-            part[i][tx] = run;
-            run += v;
-        }
-        if (e < a.E) a.recv_cnt[e] = run;
-    }
-    __syncthreads();
-    if (e < a.E) {
-        int run = part[ty][tx];
-        for (int b = b0; b < b1; ++b) {
-            const int64_t idx = (int64_t)b * a.E + e;
-            const int v = a.blk_hist[idx];
-            a.blk_hist[idx] = run;
-            if (b % a.C == 0) a.src_prefix[(int64_t)(b / a.C) * a.E + e] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    if (e < a.E) {
-        for (int s = ty; s < a.R; s += 32) {
-            const int next = (s + 1 < a.R) ? a.src_prefix[(int64_t)(s + 1) * a.E + e] : a.recv_cnt[e];
-            a.cnt[(int64_t)s * a.E + e] = next - a.src_prefix[(int64_t)s * a.E + e];
-        }
-    }
-    // num_tokens_per_rank[s][j] = sum over the rank's CTAs, one warp per (s, j)
-    const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t g = gwarp; g < (int64_t)a.R * a.R; g += nwarps) {
-        const int s = (int)(g / a.R), j = (int)(g - (int64_t)s * a.R);
-        int acc = 0;
-        for (int c = tx; c < a.C; c += 32) acc += a.blk_rank[((int64_t)s * a.C + c) * a.R + j];
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
-        if (tx == 0) a.ntpr[g] = acc;
-    }
 }
 
 // Exclusive scan of vals[0..n) into out[0..n] (out[n] = total), one CTA.
@@ -154,6 +104,43 @@ __device__ void block_exclusive_scan(const int* vals, int* out, int n, int* scra
     }
     if (tid == 0) out[n] = scratch[nt >> 5];
     __syncthreads();
+}
+
+// CTAs [0, E): the column of expert e; CTAs from E on: num_tokens_per_rank.
+// Dynamic shared memory: 2 * B + 1 + kLayoutThreads / 32 + 1 ints.
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_scan_kernel(LayoutArgs a) {
+    extern __shared__ int sm[];
+    const int B = a.B;
+    if ((int)blockIdx.x < a.E) {
+        const int e = blockIdx.x;
+        int* vals = sm;                 // [B]
+        int* pre = sm + B;              // [B+1]
+        int* scratch = pre + B + 1;     // [NW+1]
+        int* col = a.blk_hist + (int64_t)e * B;
+        for (int b = threadIdx.x; b < B; b += blockDim.x) vals[b] = col[b];
+        __syncthreads();
+        block_exclusive_scan(vals, pre, B, scratch);
+        for (int b = threadIdx.x; b < B; b += blockDim.x) col[b] = pre[b];
+        for (int s = threadIdx.x; s < a.R; s += blockDim.x) {
+            const int p0 = pre[s * a.C], p1 = pre[(s + 1) * a.C];
+            a.src_prefix[(int64_t)s * a.E + e] = p0;
+            a.cnt[(int64_t)s * a.E + e] = p1 - p0;
+        }
+        if (threadIdx.x == 0) a.recv_cnt[e] = pre[B];
+        return;
+    }
+    // num_tokens_per_rank[s][j] = sum over the rank's CTAs, one warp per (s, j)
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = ((int64_t)(blockIdx.x - a.E) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)(gridDim.x - a.E) * blockDim.x) >> 5;
+    for (int64_t g = gwarp; g < (int64_t)a.R * a.R; g += nwarps) {
+        const int s = (int)(g / a.R), j = (int)(g - (int64_t)s * a.R);
+        int acc = 0;
+        for (int c = lane; c < a.C; c += 32) acc += a.blk_rank[((int64_t)s * a.C + c) * a.R + j];
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (lane == 0) a.ntpr[g] = acc;
+    }
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
@@ -232,7 +219,7 @@ layout_assign_kernel(LayoutArgs a) {
     __syncthreads();
     // phase B: first row of each (warp, expert) = expert base + CTA prefix + earlier warps
     for (int e = tid; e < E; e += blockDim.x) {
-        int run = base[e] + a.blk_hist[(int64_t)b * E + e];
+        int run = base[e] + a.blk_hist[(int64_t)e * a.B + b];
         for (int w = 0; w < NW; ++w) {
             const int v = wc[w * E + e];
             wc[w * E + e] = run;
@@ -282,7 +269,11 @@ cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, cudaStream_t 
     const size_t smem_count = sizeof(int) * (size_t)(h->E + h->R);
     layout_count_kernel<<<h->B, kLayoutThreads, smem_count, st>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    layout_scan_kernel<<<(h->E + 31) / 32, 1024, 0, st>>>(a);
+    const int64_t pairs = (int64_t)h->R * h->R;
+    int64_t rank_ctas = (pairs + (kLayoutThreads / 32) - 1) / (kLayoutThreads / 32);
+    if (rank_ctas > 1024) rank_ctas = 1024;
+    const size_t smem_scan = sizeof(int) * (size_t)(2 * h->B + 1 + kLayoutThreads / 32 + 1);
+    layout_scan_kernel<<<(unsigned)(h->E + rank_ctas), kLayoutThreads, smem_scan, st>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     constexpr int NW = kLayoutThreads / 32;
     const size_t smem_assign = sizeof(int) * (size_t)(3 * h->E + 1 + NW + 1 + NW * h->E);
