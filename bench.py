@@ -167,6 +167,21 @@ def nvsmi_index(dev: int) -> int:
     return dev
 
 
+def max_over_ranks(values, world):
+    """Element-wise max of per-rank timings (the slowest replica sets the job's
+    time); identity on one rank.  Uses the already-initialised process group."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(world, tokens_per_replica, ms_per_step):
+    """Whole-job tokens/s: every replica processes its own full workload per step."""
+    return world * tokens_per_replica / (ms_per_step / 1e3)
+
+
 # --------------------------------------------------------------------- workload
 
 def make_inputs(w, device):
@@ -418,16 +433,12 @@ def main(argv=None):
         torch.distributed.init_process_group("gloo", timeout=datetime.timedelta(minutes=10))
     res = run_ours(args, w, quant, rank, local_rank, world)
     K = args.steps
+    res["total_ms"], e2e_ms = max_over_ranks(
+        [res["total_ms"], res["e2e"]["ms"] if res["e2e"] else 0.0], world)
+    if res["e2e"]:
+        res["e2e"]["ms"] = e2e_ms
     ms = res["total_ms"] / K
-    # max over ranks
-    if world > 1:
-        t = torch.tensor([res["total_ms"], res["e2e"]["ms"] if res["e2e"] else 0.0], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        res["total_ms"], e2e_ms = float(t[0]), float(t[1])
-        if res["e2e"]:
-            res["e2e"]["ms"] = e2e_ms
-        ms = res["total_ms"] / K
-    value = world * w.N / (ms / 1e3)
+    value = job_throughput(world, w.N, ms)
 
     peak, peak_src = measured_peaks()
     avg = {k: statistics.fmean(v) for k, v in res["phase"].items()}
