@@ -34,8 +34,13 @@ _LIB_PATH = os.path.join(_OUT_DIR, "libeporacle.so")
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 # quant-mode numbers of the C-ABI enum
-Q_NONE, Q_INT8, Q_E4M3, Q_E5M2, Q_E2M1 = 0, 2, 4, 5, 6
-QUANT_MODES = (Q_NONE, Q_INT8, Q_E4M3, Q_E5M2, Q_E2M1)
+Q_NONE, Q_INT8_STATIC, Q_INT8, Q_E4M3, Q_E5M2, Q_E2M1 = 0, 1, 2, 4, 5, 6
+Q_FP8T_E4M3, Q_FP8T_E5M2, Q_FP8G_E4M3, Q_FP8G_E5M2 = 7, 8, 9, 10
+QUANT_MODES = (Q_NONE, Q_INT8_STATIC, Q_INT8, Q_E4M3, Q_E5M2, Q_E2M1,
+               Q_FP8T_E4M3, Q_FP8T_E5M2, Q_FP8G_E4M3, Q_FP8G_E5M2)
+# kinds of the input scales of quantModes 1-3
+S_NONE, S_SCALAR, S_CHANNEL, S_EXPERT = 0, 1, 2, 3
+GROUP = 128
 
 _lock = threading.Lock()
 _lib = None
@@ -90,6 +95,14 @@ def _declare(lib):
     lib.oracle_expert_rows.argtypes = [i64, vp, vp, i32, i32, vp, vp, i32, vp]
     lib.oracle_combine.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp]
     lib.oracle_combine_ref64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp, vp]
+    lib.oracle_quant_fp8_token_row.argtypes = [i32, i32, vp, vp, vp, vp]
+    lib.oracle_quant_fp8_group_row.argtypes = [i32, i32, vp, vp, vp, vp]
+    lib.oracle_quant_int8_static_row.argtypes = [i32, vp, vp, vp]
+    lib.oracle_quant_int8_row_scaled.argtypes = [i32, vp, vp, vp, vp]
+    lib.oracle_encode_row_scaled.argtypes = [i32, i32, vp, vp, vp, vp]
+    lib.oracle_dispatch_scaled.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, i32, i64, i64, vp, vp]
+    lib.oracle_layout_masked.argtypes = [i32, i32, i32, i32, i32, vp, vp, i32, i64] + [vp] * 12
+    lib.oracle_layout_masked.restype = i32
     return lib
 
 
@@ -141,6 +154,53 @@ def quant_mx_row(q: int, x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
+def _scale_arr(smooth, H):
+    return None if smooth is None else np.ascontiguousarray(np.broadcast_to(
+        np.asarray(smooth, np.float32), (H,)), dtype=np.float32)
+
+
+def quant_fp8_token_row(fp8: int, x_bf16: np.ndarray, smooth=None):
+    """Per-token FP8 (quantMode 2, FP8 destination): (codes [H] u8, inv f32)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    H = x.shape[-1]
+    codes = np.zeros(H, np.uint8)
+    inv = np.zeros(1, np.float32)
+    sm = _scale_arr(smooth, H)
+    load().oracle_quant_fp8_token_row(H, fp8, _p(x), _p(sm), _p(codes), _p(inv))
+    return codes, inv[0]
+
+
+def quant_fp8_group_row(fp8: int, x_bf16: np.ndarray, smooth=None):
+    """Per-group-128 FP8 (quantMode 3): (codes [H] u8, inv [H/128] f32)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    H = x.shape[-1]
+    codes = np.zeros(H, np.uint8)
+    inv = np.zeros(H // GROUP, np.float32)
+    sm = _scale_arr(smooth, H)
+    load().oracle_quant_fp8_group_row(H, fp8, _p(x), _p(sm), _p(codes), _p(inv))
+    return codes, inv
+
+
+def quant_int8_static_row(x_bf16: np.ndarray, smooth) -> np.ndarray:
+    """Static int8 (quantMode 1): codes of x * scales, saturated to [-128, 127]."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    H = x.shape[-1]
+    q = np.zeros(H, np.int8)
+    load().oracle_quant_int8_static_row(H, _p(x), _p(_scale_arr(smooth, H)), _p(q))
+    return q
+
+
+def encode_row(q: int, x_bf16: np.ndarray, smooth=None):
+    """Receive-row bytes (data, scale) of one source row, optional smooth scales."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    H = x.shape[-1]
+    db, sb = row_bytes(q, H)
+    data = np.zeros(db, np.uint8)
+    scale = np.zeros(max(sb, 1), np.uint8)
+    load().oracle_encode_row_scaled(q, H, _p(x), _p(_scale_arr(smooth, H)), _p(data), _p(scale))
+    return data, scale[:sb]
+
+
 # ---------------------------------------------------------------------------
 # layout
 # ---------------------------------------------------------------------------
@@ -157,7 +217,9 @@ class Layout:
 
 
 def layout(R: int, T: int, E: int, K: int, alpha: int, topk: np.ndarray,
-           recv_cap: int | None = None) -> Layout:
+           recv_cap: int | None = None, mask: np.ndarray | None = None) -> Layout:
+    """Layout of topk; mask (xActiveMask) is [R, T] (1-D per token) or
+    [R, T, K] (2-D per entry), nonzero = active, or None."""
     topk = np.ascontiguousarray(topk, dtype=np.int64).reshape(R * T * K)
     L = E // R
     if recv_cap is None:
@@ -176,11 +238,16 @@ def layout(R: int, T: int, E: int, K: int, alpha: int, topk: np.ndarray,
         expert_ids=np.zeros((R, L), np.int32),
         expert_usage_stats=np.zeros((R, 2), np.int32),
     )
-    st = load().oracle_layout(
-        R, T, E, K, alpha, _p(topk), recv_cap,
-        *(_p(out[k]) for k in ("cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt",
-                               "aligned", "expert_start", "rank_base", "src_prefix", "dst_row",
-                               "recv_src", "expert_ids", "expert_usage_stats")))
+    outs = (_p(out[k]) for k in ("cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt",
+                                 "aligned", "expert_start", "rank_base", "src_prefix", "dst_row",
+                                 "recv_src", "expert_ids", "expert_usage_stats"))
+    if mask is None:
+        st = load().oracle_layout(R, T, E, K, alpha, _p(topk), recv_cap, *outs)
+    else:
+        m = np.ascontiguousarray(mask, dtype=np.uint8)
+        dims = 1 if m.size == R * T else 2
+        assert m.size == (R * T if dims == 1 else R * T * K)
+        st = load().oracle_layout_masked(R, T, E, K, alpha, _p(topk), _p(m), dims, recv_cap, *outs)
     rows = int(out["rank_base"][-1])
     out["recv_src"] = out["recv_src"][: min(rows, recv_cap)]
     return Layout(status=int(st), R=R, T=T, E=E, K=K, alpha=alpha, L=L, **out)
@@ -212,6 +279,28 @@ def dispatch(lay: Layout, x_bf16: np.ndarray, q: int, row_begin: int = 0,
     load().oracle_dispatch(N, lay.K, H, q, _p(dr), _p(x), row_begin, row_end, _p(data),
                            _p(scales) if sb else None)
     return data, scales
+
+
+def dispatch_scaled(lay: Layout, x_bf16: np.ndarray, q: int, topk: np.ndarray,
+                    scales: np.ndarray | None, kind: int, row_begin: int = 0,
+                    row_end: int | None = None):
+    """Receive rows with input scales of a kind (S_SCALAR [1], S_CHANNEL [H],
+    S_EXPERT [E, H]); quantModes 1-3 only."""
+    N = lay.R * lay.T
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    H = x.shape[1]
+    if row_end is None:
+        row_end = lay.rows
+    db, sb = row_bytes(q, H)
+    n = row_end - row_begin
+    data = np.zeros((n, db), np.uint8)
+    scl = np.zeros((n, sb), np.uint8)
+    dr = np.ascontiguousarray(lay.dst_row.reshape(-1))
+    tk = np.ascontiguousarray(topk, dtype=np.int64).reshape(-1)
+    sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
+    load().oracle_dispatch_scaled(N, lay.K, H, q, _p(dr), _p(tk), _p(x), _p(sc), kind, row_begin,
+                                  row_end, _p(data), _p(scl) if sb else None)
+    return data, scl
 
 
 def dispatch_rows(lay: Layout, x_bf16: np.ndarray, q: int, rows: np.ndarray):

@@ -14,9 +14,12 @@
  *       return values recv_x formats and num_recv_tokens_per_expert_list
  *       ("aligned"), and combine ("multiply by weights and sum").
  *   - "aclnnMoeDistributeDispatchV2" (CANN), Formula section: quantMode 0
- *       (no quant), quantMode 2 (per-token dynamic int8), quantMode 4 (MX,
- *       sharedExp = floor(log2(max)) - emax), and the constraint that
- *       localExpertNum = moeExpertNum / epWorldSize.
+ *       (no quant), quantMode 1 (static, int8, with scales of shape (1,),
+ *       (H,) or (E,H)), quantMode 2 (per-token dynamic, int8 or FP8
+ *       destination), quantMode 3 (per-group dynamic, FP8), quantMode 4 (MX,
+ *       sharedExp = floor(log2(max)) - emax), optional smooth scales
+ *       (xFp32 = CastToFp32(X) x scales) for quantModes 1-3, xActiveMask, and
+ *       the constraint that localExpertNum = moeExpertNum / epWorldSize.
  *   - "max.nn.comm.ep.EPBatchManager" (Modular MAX): ep_dispatch outputs
  *       (expert_start_indices, expert_ids, expert_usage_stats) and ep_combine
  *       (weighted sum of routed outputs plus fused shared-expert outputs).
@@ -28,7 +31,8 @@
  * = fl(1/s); MX amax over each 32-element block of |x|; e8m0 byte = se + 127
  * (the decode scale 2^se); fp8/fp4 casts round to nearest even and saturate
  * to the largest finite value, keeping the sign of zero; e2m1 element 2i in
- * the low nibble of byte i.
+ * the low nibble of byte i; per-group quantisation uses groups of 128
+ * elements; static int8 saturates to [-128, 127].
  *
  * Compile without FMA contraction or fast-math:
  *   gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared
@@ -42,7 +46,16 @@
 
 /* Quant modes, numbered as in the C-ABI header's enum (the values are part of
  * the interface contract, not shared code). */
-enum { Q_NONE = 0, Q_INT8 = 2, Q_E4M3 = 4, Q_E5M2 = 5, Q_E2M1 = 6 };
+enum { Q_NONE = 0, Q_INT8_STATIC = 1, Q_INT8 = 2, Q_E4M3 = 4, Q_E5M2 = 5, Q_E2M1 = 6,
+       Q_FP8T_E4M3 = 7, Q_FP8T_E5M2 = 8, Q_FP8G_E4M3 = 9, Q_FP8G_E5M2 = 10 };
+
+/* Kinds of the optional input scales of quantModes 1-3 (CANN: a scalar (1,), a
+ * smooth weight shared by all experts (H,), or one row per expert (E, H)). */
+enum { S_NONE = 0, S_SCALAR = 1, S_CHANNEL = 2, S_EXPERT = 3 };
+
+/* Elements per group of the per-group dynamic quantisation (quantMode 3);
+ * the page's per-group buffer rule aligns H to 128. */
+#define GROUP 128
 
 /* Status values returned by oracle_layout. */
 enum { O_OK = 0, O_CAPACITY = 3, O_BAD_EXPERT = 4 };
@@ -162,24 +175,36 @@ static float round_half_even(float v) {
 /* An all-zero row has dynamicScales = +inf; its codes are 0 and its sent    */
 /* scale is 1/inf = 0.                                                       */
 /* ------------------------------------------------------------------------ */
-void oracle_quant_int8_row(int H, const uint16_t* x, int8_t* q, float* inv) {
+/* The scaled input of quantModes 1-3: xFp32 = CastToFp32(X) x scales, one
+ * factor per element (smooth == NULL: no scales, factor 1, no multiply). */
+static float scaled_x(const uint16_t* x, const float* smooth, int h) {
+    float v = oracle_bf16_to_f32(x[h]);
+    return smooth ? v * smooth[h] : v;
+}
+
+/* Per-token int8 with optional smooth scales (the row multiplied by them
+ * first). */
+void oracle_quant_int8_row_scaled(int H, const uint16_t* x, const float* smooth, int8_t* q, float* inv) {
     float amax = 0.0f;
     for (int h = 0; h < H; ++h) {
-        float a = fabsf(oracle_bf16_to_f32(x[h]));
+        float a = fabsf(scaled_x(x, smooth, h));
         if (a > amax) amax = a;
     }
     float s = 127.0f / amax;
     for (int h = 0; h < H; ++h) {
         float r = 0.0f;
         if (amax > 0.0f) {
-            float v = oracle_bf16_to_f32(x[h]) * s;
-            r = round_half_even(v);
+            r = round_half_even(scaled_x(x, smooth, h) * s);
             if (r > 127.0f) r = 127.0f;
             if (r < -127.0f) r = -127.0f;
         }
         q[h] = (int8_t)(int)r;
     }
     *inv = 1.0f / s;
+}
+
+void oracle_quant_int8_row(int H, const uint16_t* x, int8_t* q, float* inv) {
+    oracle_quant_int8_row_scaled(H, x, NULL, q, inv);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -224,6 +249,61 @@ void oracle_quant_mx_row(int H, int q, const uint16_t* x, uint8_t* codes, uint8_
     }
 }
 
+/* CANN Formula, Case 3 with an FP8 destination (quantMode 2, FLOAT8_E4M3FN or
+ * FLOAT8_E5M2): dynamicScales = dstTypeMax / Max(Abs(xFp32)) over the row,
+ * quantOut = Cast(xFp32 * dynamicScales) (round to nearest even, saturate),
+ * sent scale 1.0 / dynamicScales.  dstTypeMax: 448 (e4m3), 57344 (e5m2).  An
+ * all-zero row gives codes 0 and scale 0. */
+void oracle_quant_fp8_token_row(int H, int fp8, const uint16_t* x, const float* smooth,
+                                uint8_t* codes, float* inv) {
+    const float dmax = (fp8 == Q_E4M3) ? 448.0f : 57344.0f;
+    float amax = 0.0f;
+    for (int h = 0; h < H; ++h) {
+        float a = fabsf(scaled_x(x, smooth, h));
+        if (a > amax) amax = a;
+    }
+    float s = dmax / amax;
+    for (int h = 0; h < H; ++h)
+        codes[h] = (amax > 0.0f) ? (uint8_t)oracle_mini_encode(fp8, scaled_x(x, smooth, h) * s) : 0;
+    *inv = 1.0f / s;
+}
+
+/* CANN Formula, Case 4 (quantMode 3, per-group dynamic; FP8 destinations):
+ * the per-token rule applied to every group of 128 consecutive elements;
+ * one float32 scale (1.0 / dynamicScales) per group. */
+void oracle_quant_fp8_group_row(int H, int fp8, const uint16_t* x, const float* smooth,
+                                uint8_t* codes, float* inv) {
+    for (int g = 0; g < H / GROUP; ++g)
+        oracle_quant_fp8_token_row(GROUP, fp8, x + g * GROUP, smooth ? smooth + g * GROUP : NULL,
+                                   codes + g * GROUP, inv + g);
+}
+
+/* CANN Formula, Case 2 (quantMode 1, static, INT8 destination):
+ * quantOut = Cast(xFp32, int8), round to nearest even, saturated to the int8
+ * range [-128, 127]; no scale is sent (the receiver knows the static scales). */
+void oracle_quant_int8_static_row(int H, const uint16_t* x, const float* smooth, int8_t* q) {
+    for (int h = 0; h < H; ++h) {
+        float r = round_half_even(scaled_x(x, smooth, h));
+        if (r > 127.0f) r = 127.0f;
+        if (r < -128.0f) r = -128.0f;
+        q[h] = (int8_t)(int)r;
+    }
+}
+
+/* Encode one row with an optional smooth-scale row (quantModes 1-3 only). */
+void oracle_encode_row_scaled(int q, int H, const uint16_t* x, const float* smooth,
+                              uint8_t* data, uint8_t* scale) {
+    switch (q) {
+        case Q_INT8_STATIC: oracle_quant_int8_static_row(H, x, smooth, (int8_t*)data); break;
+        case Q_INT8: oracle_quant_int8_row_scaled(H, x, smooth, (int8_t*)data, (float*)scale); break;
+        case Q_FP8T_E4M3: oracle_quant_fp8_token_row(H, Q_E4M3, x, smooth, data, (float*)scale); break;
+        case Q_FP8T_E5M2: oracle_quant_fp8_token_row(H, Q_E5M2, x, smooth, data, (float*)scale); break;
+        case Q_FP8G_E4M3: oracle_quant_fp8_group_row(H, Q_E4M3, x, smooth, data, (float*)scale); break;
+        case Q_FP8G_E5M2: oracle_quant_fp8_group_row(H, Q_E5M2, x, smooth, data, (float*)scale); break;
+        default: break;
+    }
+}
+
 /* Bytes of one receive row's data and scale parts for a quant mode. */
 int64_t oracle_row_data_bytes(int q, int H) {
     if (q == Q_NONE) return 2 * (int64_t)H;
@@ -231,8 +311,9 @@ int64_t oracle_row_data_bytes(int q, int H) {
     return H;
 }
 int64_t oracle_row_scale_bytes(int q, int H) {
-    if (q == Q_NONE) return 0;
-    if (q == Q_INT8) return 4;
+    if (q == Q_NONE || q == Q_INT8_STATIC) return 0;
+    if (q == Q_INT8 || q == Q_FP8T_E4M3 || q == Q_FP8T_E5M2) return 4;
+    if (q == Q_FP8G_E4M3 || q == Q_FP8G_E5M2) return 4 * (H / GROUP);
     return H / 32;
 }
 
@@ -240,7 +321,8 @@ int64_t oracle_row_scale_bytes(int q, int H) {
 void oracle_encode_row(int q, int H, const uint16_t* x, uint8_t* data, uint8_t* scale) {
     if (q == Q_NONE) memcpy(data, x, 2 * (size_t)H);
     else if (q == Q_INT8) oracle_quant_int8_row(H, x, (int8_t*)data, (float*)scale);
-    else oracle_quant_mx_row(H, q, x, data, scale);
+    else if (q == Q_E4M3 || q == Q_E5M2 || q == Q_E2M1) oracle_quant_mx_row(H, q, x, data, scale);
+    else oracle_encode_row_scaled(q, H, x, NULL, data, scale);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -361,6 +443,30 @@ int oracle_layout(int R, int T, int E, int K, int alpha, const int64_t* topk,
     return status;
 }
 
+/* xActiveMask (CANN aclnnMoeDistributeDispatchV2): a false token (1-D mask,
+ * [R*T]) or a false entry (2-D mask, [R*T*K]) does not take part in the
+ * communication -- it is laid out exactly like an entry whose topk id is -1.
+ * The page asks 1-D masks to be a prefix of true values; any pattern gives a
+ * well-defined layout here. */
+int oracle_layout_masked(int R, int T, int E, int K, int alpha, const int64_t* topk,
+                         const uint8_t* mask, int mask_dims, int64_t recv_cap,
+                         int32_t* cnt, uint8_t* itr, int32_t* ntpr,
+                         int32_t* recv_cnt, int32_t* aligned,
+                         int32_t* expert_start, int64_t* rank_base,
+                         int32_t* src_prefix, int32_t* dst_row, int32_t* recv_src,
+                         int32_t* expert_ids, int32_t* usage) {
+    int64_t n_ent = (int64_t)R * T * K;
+    int64_t* t2 = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_ent > 0 ? n_ent : 1));
+    for (int64_t i = 0; i < n_ent; ++i) {
+        int active = (mask_dims == 1) ? mask[i / K] : mask[i];
+        t2[i] = active ? topk[i] : -1;
+    }
+    int st = oracle_layout(R, T, E, K, alpha, t2, recv_cap, cnt, itr, ntpr, recv_cnt, aligned,
+                           expert_start, rank_base, src_prefix, dst_row, recv_src, expert_ids, usage);
+    free(t2);
+    return st;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Dispatch: every valid entry (s,t,k) receives the encoded row of token     */
 /* (s,t) at dst_row[s,t,k]; padding rows are all-zero bytes.                */
@@ -387,6 +493,41 @@ void oracle_dispatch(int N, int K, int H, int q, const int32_t* dst_row,
     }
     free(tmp_d);
     free(tmp_s);
+}
+
+/* Dispatch with input scales (quantModes 1-3): as oracle_dispatch, but each
+ * entry's row is encoded with the scale row that applies to it: the scalar
+ * scale[0] for every element (S_SCALAR), the shared row scale[0..H)
+ * (S_CHANNEL), or the row of the entry's expert scale[e*H .. e*H+H) (S_EXPERT,
+ * e = topk[s,t,k]).  S_NONE is oracle_dispatch. */
+void oracle_dispatch_scaled(int N, int K, int H, int q, const int32_t* dst_row, const int64_t* topk,
+                            const uint16_t* x, const float* scales, int kind,
+                            int64_t row_begin, int64_t row_end,
+                            uint8_t* recv_data, uint8_t* recv_scales) {
+    int64_t db = oracle_row_data_bytes(q, H), sb = oracle_row_scale_bytes(q, H);
+    memset(recv_data, 0, (size_t)((row_end - row_begin) * db));
+    if (sb) memset(recv_scales, 0, (size_t)((row_end - row_begin) * sb));
+    float* row = (float*)malloc(sizeof(float) * (size_t)H);
+    for (int64_t n = 0; n < N; ++n) {
+        for (int k = 0; k < K; ++k) {
+            int64_t d = dst_row[n * K + k];
+            if (d < row_begin || d >= row_end) continue;
+            const float* sm = NULL;
+            if (kind == S_SCALAR) {
+                for (int h = 0; h < H; ++h) row[h] = scales[0];
+                sm = row;
+            } else if (kind == S_CHANNEL) {
+                sm = scales;
+            } else if (kind == S_EXPERT) {
+                sm = scales + topk[n * K + k] * (int64_t)H;
+            }
+            uint8_t* dd = recv_data + (d - row_begin) * db;
+            uint8_t* ds = sb ? recv_scales + (d - row_begin) * sb : NULL;
+            if (q == Q_INT8_STATIC || q == Q_INT8 || q >= Q_FP8T_E4M3) oracle_encode_row_scaled(q, H, x + n * H, sm, dd, ds);
+            else oracle_encode_row(q, H, x + n * H, dd, ds);
+        }
+    }
+    free(row);
 }
 
 /* The same receive rows, produced one by one for a list of row indices via
@@ -432,6 +573,13 @@ void oracle_expert_rows(int64_t nrows, const int64_t* rows, const int32_t* row_e
             } else if (q == Q_INT8) {
                 float inv; memcpy(&inv, s, 4);
                 v = (float)(int8_t)d[h] * inv;
+            } else if (q == Q_FP8T_E4M3 || q == Q_FP8T_E5M2 || q == Q_FP8G_E4M3 || q == Q_FP8G_E5M2) {
+                int fp8 = (q == Q_FP8T_E4M3 || q == Q_FP8G_E4M3) ? Q_E4M3 : Q_E5M2;
+                float inv;
+                memcpy(&inv, s + ((q == Q_FP8G_E4M3 || q == Q_FP8G_E5M2) ? 4 * (h / GROUP) : 0), 4);
+                v = (float)oracle_mini_decode(fp8, d[h]) * inv;
+            } else if (q == Q_INT8_STATIC) {
+                v = (float)(int8_t)d[h];
             } else {
                 int code = (q == Q_E2M1) ? ((d[h / 2] >> (4 * (h & 1))) & 0xf) : d[h];
                 float dyn = ldexpf(1.0f, (int)s[h / 32] - 127);

@@ -16,6 +16,7 @@ import oracle
 import test_oracle_dispatch_combine as tdc
 import test_oracle_layout as tl
 import test_oracle_quant as tq
+import test_oracle_quant_ext as tqx
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ep_oracle.c")
 
@@ -30,7 +31,8 @@ MUTANTS = {
     "layout_transposed_expert_map": ("int j = (int)(e / L), l = (int)(e % L);",
                                      "int j = (int)(e % R), l = (int)(e / R);"),
     "int8_wrong_type_max": ("float s = 127.0f / amax;", "float s = 128.0f / amax;"),
-    "int8_inverse_as_amax_over_127": ("*inv = 1.0f / s;", "*inv = amax / 127.0f;"),
+    "int8_inverse_as_amax_over_127": ("        q[h] = (int8_t)(int)r;\n    }\n    *inv = 1.0f / s;",
+                                      "        q[h] = (int8_t)(int)r;\n    }\n    *inv = amax / 127.0f;"),
     "int8_round_half_up": ("return (fmodf(f, 2.0f) == 0.0f) ? f : f + 1.0f;", "return f + 1.0f;"),
     "mx_exponent_off_by_one": ("se = (expfield - 127) - m.emax;", "se = (expfield - 127) - m.emax + 1;"),
     "mx_e2m1_nibble_swap": ("codes[h / 2] |= (uint8_t)(c << (4 * (h & 1)));",
@@ -42,6 +44,16 @@ MUTANTS = {
     "bf16_ties_up": ("else pick = (lo & 1u) ? hi : lo;", "else pick = hi;"),
     "combine_first_weight_only": ("float prod = w[n * K + k] * oracle_bf16_to_f32(y[yr * H + h]);",
                                   "float prod = w[n * K] * oracle_bf16_to_f32(y[yr * H + h]);"),
+    "fp8_token_wrong_type_max": ("const float dmax = (fp8 == Q_E4M3) ? 448.0f : 57344.0f;",
+                                 "const float dmax = (fp8 == Q_E4M3) ? 480.0f : 57344.0f;"),
+    "fp8_group_drops_last_group": ("for (int g = 0; g < H / GROUP; ++g)\n        oracle_quant_fp8_token_row(",
+                                   "for (int g = 0; g < H / GROUP - 1; ++g)\n        oracle_quant_fp8_token_row("),
+    "int8_static_symmetric_saturation": ("if (r < -128.0f) r = -128.0f;", "if (r < -127.0f) r = -127.0f;"),
+    "scaled_first_slot_expert": ("sm = scales + topk[n * K + k] * (int64_t)H;",
+                                 "sm = scales + topk[n * K] * (int64_t)H;"),
+    "mask_token_index": ("int active = (mask_dims == 1) ? mask[i / K] : mask[i];",
+                         "int active = (mask_dims == 1) ? mask[i % (R * T)] : mask[i];"),
+    "smooth_scales_ignored": ("return smooth ? v * smooth[h] : v;", "return v;"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -63,6 +75,13 @@ def pins():
               lambda: tq.test_fp8_encode_matches_torch_in_range("e4m3", torch.float8_e4m3fn, 0x7e)]
     cases += [lambda: tdc.test_combine_identity_and_marked_experts(1, 64, 4),
               lambda: tdc.test_combine_identity_and_marked_experts(5, 8, 0)]
+    cases += [lambda c=c: tqx.test_golden(c) for c in tq.read_cases("fp8_static_rows.txt")]
+    cases += [lambda: tqx.test_fp8_token_exact_route(oracle.Q_FP8T_E4M3),
+              lambda: tqx.test_fp8_group_exact_route(oracle.Q_FP8G_E4M3),
+              tqx.test_int8_static_exact_route, tqx.test_smooth_scales_exact_route_fp8,
+              lambda: tqx.test_dispatch_per_expert_scales_pick_the_entrys_expert(oracle.Q_INT8),
+              lambda: tqx.test_masked_layout_matches_brute_force(0),
+              lambda: tqx.test_masked_layout_matches_brute_force(1)]
     return cases
 
 
