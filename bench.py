@@ -38,8 +38,17 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s vs GB300 peak, 1 GPU"
-WORKLOAD_KEYS = {"1": (1, 0), "2": (2, 0), "3": (3, 2), "4a": (4, 4), "4b": (4, 6), "5": (5, 0)}
-QNAME = {0: "none", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2", 6: "mxfp4_e2m1"}
+# key -> (workload index, quant mode, input-scale kind, xActiveMask dims)
+WORKLOAD_KEYS = {"1": (1, 0, 0, 0), "2": (2, 0, 0, 0), "3": (3, 2, 0, 0), "4a": (4, 4, 0, 0),
+                 "4b": (4, 6, 0, 0), "5": (5, 0, 0, 0),
+                 # further CANN quant modes and xActiveMask on the same shapes
+                 "4t": (4, 7, 0, 0), "4g": (4, 9, 0, 0), "3s": (3, 1, 2, 0), "3e": (3, 2, 3, 0),
+                 "5m": (5, 0, 0, 2)}
+QNAME = {0: "none", 1: "int8_static", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2",
+         6: "mxfp4_e2m1", 7: "fp8_e4m3_per_token", 8: "fp8_e5m2_per_token",
+         9: "fp8_e4m3_per_group128", 10: "fp8_e5m2_per_group128"}
+SCALE_KIND = {0: "none", 1: "scalar", 2: "per_channel", 3: "per_expert"}
+SAMPLE_NOTE = " (input scales and xActiveMask are not applied in the oracle sample)"
 KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "layout": "layout.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
@@ -203,15 +212,22 @@ def algorithmic_bytes(w, quant, rows, V):
     return {"layout": lay, "dispatch": disp, "combine": comb}
 
 
-def run_ours(args, w, quant, rank, local_rank, world):
-    from combine_ep_layout_03_gb300 import ep
+def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0):
+    from combine_ep_layout_03_gb300 import ep, synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     topk, wts, x_dev, sh_dev = make_inputs(w, dev)
     topk_dev = torch.from_numpy(topk).to(dev)
     w_dev = torch.from_numpy(wts).to(dev)
+    sc = synth.gen_scales(w, kind)
+    sc_dev = None if sc is None else torch.from_numpy(sc).to(dev)
+    mask_dev = None if not mask_dims else torch.from_numpy(synth.gen_mask(w, mask_dims)).to(dev)
+    if mask_dev is not None:
+        # masked entries carry no weight, like topk -1 entries
+        m3 = mask_dev.bool().view(w.R, w.T, -1).expand(w.R, w.T, w.K) if mask_dims == 1 else mask_dev.bool()
+        w_dev = torch.where(m3.reshape(w_dev.shape), w_dev, torch.zeros_like(w_dev))
     lay = ep.EPLayout(w.R, w.T, w.H, w.E, w.K, w.alpha, device=dev)
-    lay.layout(topk_dev)
+    lay.layout(topk_dev, active_mask=mask_dev)
     rank_base = lay.recv_rows()
     rows = int(rank_base[-1])
     V = int((topk >= 0).sum())
@@ -219,7 +235,7 @@ def run_ours(args, w, quant, rank, local_rank, world):
     if quant == 0:
         y = data.view(torch.bfloat16).view(-1, w.H)
     else:
-        lay.dispatch(x_dev, quant, data, scales)
+        lay.dispatch(x_dev, quant, data, scales, scales=sc_dev, scale_kind=kind)
         y = torch.empty((max(rows, 1), w.H), dtype=torch.bfloat16, device=dev)
         lay.expert_identity(quant, data, scales, y)
     out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
@@ -228,10 +244,10 @@ def run_ours(args, w, quant, rank, local_rank, world):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        lay.layout(topk_dev)
+        lay.layout(topk_dev, active_mask=mask_dev)
         if ev is not None:
             ev[1].record(stream)
-        lay.dispatch(x_dev, quant, data, scales)
+        lay.dispatch(x_dev, quant, data, scales, scales=sc_dev, scale_kind=kind)
         if ev is not None:
             ev[2].record(stream)
         lay.combine(y, w_dev, out, sh_dev)
@@ -310,8 +326,8 @@ def run_ours(args, w, quant, rank, local_rank, world):
                 s_k.wait_event(ev_in[i])
                 if i >= 2:
                     s_k.wait_event(ev_out[i - 2])         # slot's output already read back
-                lay.layout(sl["topk"], s_k)
-                lay.dispatch(sl["x"], quant, data, scales, s_k)
+                lay.layout(sl["topk"], s_k, active_mask=mask_dev)
+                lay.dispatch(sl["x"], quant, data, scales, s_k, scales=sc_dev, scale_kind=kind)
                 lay.combine(y, sl["w"], sl["out"], sl["sh"], s_k)
                 ev_k[i].record(s_k)
                 with torch.cuda.stream(s_out):
@@ -403,9 +419,9 @@ def host_shared_lead(sh_dev, w, ranks=2):
 
 # --------------------------------------------------------------------- main
 
-def workload_config(w, quant, key):
-    from combine_ep_layout_03_gb300 import synth
+def workload_config(w, quant, key, kind=0, mask_dims=0):
     return {"workload": f"ep_layout_dispatch_combine[{key}] " + w.name,
+            "input_scales": SCALE_KIND[kind], "active_mask_dims": mask_dims,
             "R": w.R, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "alpha": w.alpha,
             "routing": w.routing, "drop_p": w.drop_p, "num_shared": w.num_shared,
             "quant": QNAME[quant], "tokens_per_step": w.N,
@@ -418,7 +434,7 @@ def main(argv=None):
     args = parse_args(argv)
     rank, local_rank, world = dist_env()
     from combine_ep_layout_03_gb300 import synth
-    idx, quant = WORKLOAD_KEYS[args.workload]
+    idx, quant, kind, mask_dims = WORKLOAD_KEYS[args.workload]
     w = synth.WORKLOADS[idx]
     if args.tokens_per_rank:
         w = w.with_(T=args.tokens_per_rank)
@@ -426,12 +442,12 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        return run_reference(args, w, quant)
+        return run_reference(args, w, quant, kind, mask_dims)
 
     if world > 1:
         import datetime
         torch.distributed.init_process_group("gloo", timeout=datetime.timedelta(minutes=10))
-    res = run_ours(args, w, quant, rank, local_rank, world)
+    res = run_ours(args, w, quant, rank, local_rank, world, kind, mask_dims)
     K = args.steps
     res["total_ms"], e2e_ms = max_over_ranks(
         [res["total_ms"], res["e2e"]["ms"] if res["e2e"] else 0.0], world)
@@ -457,7 +473,7 @@ def main(argv=None):
         sh0 = host_shared_lead(res["sh_dev"], w)
         v, desc, spent, n = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget)
         cpu = {"value": round(v, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": desc}
+               "sample": desc + SAMPLE_NOTE * bool(kind or mask_dims)}
 
     e2e = None
     if res["e2e"]:
@@ -474,7 +490,7 @@ def main(argv=None):
         "dtype": "bf16" if quant == 0 else f"bf16->{QNAME[quant]}",
         "data": "synthetic (seeded: x ~ N(0,1) rounded to bf16, routing and softmax weights per "
                 "the workload's recipe; identity experts)",
-        "config": workload_config(w, quant, args.workload),
+        "config": workload_config(w, quant, args.workload, kind, mask_dims),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -493,7 +509,7 @@ def main(argv=None):
     return 0
 
 
-def run_reference(args, w, quant):
+def run_reference(args, w, quant, kind=0, mask_dims=0):
     """The CPU oracle as the reference arm: each step times the oracle on a
     bounded sample of the same workload, on the host cores."""
     from combine_ep_layout_03_gb300 import synth
@@ -516,9 +532,9 @@ def run_reference(args, w, quant):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if quant == 0 else f"bf16->{QNAME[quant]}",
         "data": "synthetic (same seeded recipe as the GPU arm)", "impl": "reference",
-        "config": workload_config(w, quant, args.workload),
+        "config": workload_config(w, quant, args.workload, kind, mask_dims),
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle", "sample": descs},
+                         "kind": "oracle", "sample": descs + SAMPLE_NOTE * bool(kind or mask_dims)},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -193,7 +193,8 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
 
 // ---------------------------------------------------------------- identity expert
 
-enum { M_NONE = 0, M_INT8 = 2, M_E4M3 = 4, M_E5M2 = 5, M_E2M1 = 6 };
+enum { M_NONE = 0, M_INT8S = 1, M_INT8 = 2, M_E4M3 = 4, M_E5M2 = 5, M_E2M1 = 6,
+       M_FP8T_E4M3 = 7, M_FP8T_E5M2 = 8, M_FP8G_E4M3 = 9, M_FP8G_E5M2 = 10 };
 
 __device__ __forceinline__ float pow2i(int e) {  // 2^e for e in [-149, 127], exact
     if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
@@ -242,6 +243,14 @@ identity_kernel(IdentityArgs a) {
                 } else if (Q == M_INT8) {
                     const float inv = reinterpret_cast<const float*>(srow)[0];
                     v = __fmul_rn((float)(int8_t)row[h], inv);
+                } else if (Q == M_INT8S) {
+                    v = (float)(int8_t)row[h];
+                } else if (Q == M_FP8T_E4M3 || Q == M_FP8T_E5M2 || Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2) {
+                    const bool grp = (Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2);
+                    const float inv = reinterpret_cast<const float*>(srow)[grp ? (h >> 7) : 0];
+                    const float cv = (Q == M_FP8T_E4M3 || Q == M_FP8G_E4M3) ? decode_mini(row[h], 4, 3, 7)
+                                                                             : decode_mini(row[h], 5, 2, 15);
+                    v = __fmul_rn(cv, inv);
                 } else {
                     uint32_t c;
                     if (Q == M_E2M1) c = (row[h >> 1] >> (4 * (h & 1))) & 0xfu;
@@ -309,6 +318,11 @@ cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant
         case M_E4M3: identity_kernel<M_E4M3><<<grid, 256, 0, st>>>(a); break;
         case M_E5M2: identity_kernel<M_E5M2><<<grid, 256, 0, st>>>(a); break;
         case M_E2M1: identity_kernel<M_E2M1><<<grid, 256, 0, st>>>(a); break;
+        case M_INT8S: identity_kernel<M_INT8S><<<grid, 256, 0, st>>>(a); break;
+        case M_FP8T_E4M3: identity_kernel<M_FP8T_E4M3><<<grid, 256, 0, st>>>(a); break;
+        case M_FP8T_E5M2: identity_kernel<M_FP8T_E5M2><<<grid, 256, 0, st>>>(a); break;
+        case M_FP8G_E4M3: identity_kernel<M_FP8G_E4M3><<<grid, 256, 0, st>>>(a); break;
+        case M_FP8G_E5M2: identity_kernel<M_FP8G_E5M2><<<grid, 256, 0, st>>>(a); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -31,7 +31,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-enum { M_NONE = 0, M_INT8 = 2, M_E4M3 = 4, M_E5M2 = 5, M_E2M1 = 6 };
+enum { M_NONE = 0, M_INT8S = 1, M_INT8 = 2, M_E4M3 = 4, M_E5M2 = 5, M_E2M1 = 6,
+       M_FP8T_E4M3 = 7, M_FP8T_E5M2 = 8, M_FP8G_E4M3 = 9, M_FP8G_E5M2 = 10 };
 
 // |bf16| of the 8 elements of a vector, as the max of the magnitude bits
 // (monotone in the value for finite inputs).
@@ -81,11 +82,20 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float f[8]) {
     return r;
 }
 
+// Per-mode constants.  token: one dynamic scale per row (CTA-wide amax);
+// group: one per 128 elements (16 lanes); fp8: element type of the FP8 modes.
 template <int Q>
-struct MxTraits { static constexpr int emax = 0; };
-template <> struct MxTraits<M_E4M3> { static constexpr int emax = 8; };
-template <> struct MxTraits<M_E5M2> { static constexpr int emax = 15; };
-template <> struct MxTraits<M_E2M1> { static constexpr int emax = 2; };
+struct QTraits {
+    static constexpr bool mx = (Q == M_E4M3 || Q == M_E5M2 || Q == M_E2M1);
+    static constexpr bool token = (Q == M_INT8 || Q == M_FP8T_E4M3 || Q == M_FP8T_E5M2);
+    static constexpr bool group = (Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2);
+    static constexpr int fp8 = (Q == M_FP8T_E4M3 || Q == M_FP8G_E4M3) ? M_E4M3 : M_E5M2;
+    // dstTypeMax of the dynamic modes (quantModes 2 and 3)
+    static constexpr float dmax = (Q == M_INT8) ? 127.0f : (fp8 == M_E4M3 ? 448.0f : 57344.0f);
+    // emax of the MX element types (quantMode 4)
+    static constexpr int emax = (Q == M_E4M3) ? 8 : (Q == M_E5M2 ? 15 : 2);
+    static constexpr int VB = (Q == M_E2M1) ? 4 : 8;  // code bytes per 8 elements
+};
 
 // Zero one padding row region [r0, r1) of data and scales with the whole CTA.
 __device__ void zero_rows(const DispatchArgs& a, int64_t r0, int64_t r1) {
@@ -106,15 +116,116 @@ __device__ void zero_rows(const DispatchArgs& a, int64_t r0, int64_t r1) {
     }
 }
 
-// Quantised rows.  BULK: the encoded row (and, for MX rows whose scale row is
-// a multiple of 16 bytes, the scale row) is written once into one of two
-// shared-memory stages and thread 0 sends it to the K destination rows with
-// cp.async.bulk stores (one bulk group per token; a stage is rewritten only
-// after wait_group.read shows the group of two tokens earlier has read it).
-// Otherwise every thread stores its codes to each destination itself.
+// Multiply the row's floats by the input scales (quantModes 1-3).
+template <int VPT>
+__device__ __forceinline__ void apply_scales(float f[VPT][8], const float* sc, int kind, int nt,
+                                             int nvec) {
+    if (kind == EP_SCALES_SCALAR) {
+        const float c = __ldg(sc);
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[u][i] = __fmul_rn(f[u][i], c);
+    } else if (kind != EP_SCALES_NONE) {  // a row of H scales
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * nt + threadIdx.x;
+            if (vi < nvec) {
+                const float4 s0 = __ldg(reinterpret_cast<const float4*>(sc) + 2 * vi);
+                const float4 s1 = __ldg(reinterpret_cast<const float4*>(sc) + 2 * vi + 1);
+                f[u][0] = __fmul_rn(f[u][0], s0.x); f[u][1] = __fmul_rn(f[u][1], s0.y);
+                f[u][2] = __fmul_rn(f[u][2], s0.z); f[u][3] = __fmul_rn(f[u][3], s0.w);
+                f[u][4] = __fmul_rn(f[u][4], s1.x); f[u][5] = __fmul_rn(f[u][5], s1.y);
+                f[u][6] = __fmul_rn(f[u][6], s1.z); f[u][7] = __fmul_rn(f[u][7], s1.w);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t absmax_bits8(const float f[8]) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = max(m, __float_as_uint(fabsf(f[i])));  // monotone for |x| >= 0
+    return m;
+}
+
+// Codes of 8 scaled elements with dynamic scale s (per-token / per-group modes).
+template <int Q>
+__device__ __forceinline__ void encode_dynamic(const float f[8], float s, bool nonzero, uint32_t out[2]) {
+    if (!nonzero) { out[0] = out[1] = 0; return; }
+    if constexpr (Q == M_INT8) {
+        out[0] = q8(f[0], s) | (q8(f[1], s) << 8) | (q8(f[2], s) << 16) | (q8(f[3], s) << 24);
+        out[1] = q8(f[4], s) | (q8(f[5], s) << 8) | (q8(f[6], s) << 16) | (q8(f[7], s) << 24);
+    } else {
+        constexpr int C = QTraits<Q>::fp8;
+        out[0] = cvt_fp8x2<C>(__fmul_rn(f[0], s), __fmul_rn(f[1], s)) |
+                 (cvt_fp8x2<C>(__fmul_rn(f[2], s), __fmul_rn(f[3], s)) << 16);
+        out[1] = cvt_fp8x2<C>(__fmul_rn(f[4], s), __fmul_rn(f[5], s)) |
+                 (cvt_fp8x2<C>(__fmul_rn(f[6], s), __fmul_rn(f[7], s)) << 16);
+    }
+}
+
+// Static int8 (quantMode 1): round half even, saturate to [-128, 127].
+__device__ __forceinline__ uint32_t q8s(float x) {
+    int q = __float2int_rn(x);
+    q = max(-128, min(127, q));
+    return (uint32_t)q & 0xffu;
+}
+
+// Per-vector encoding of every mode except the CTA-wide amax step: MX blocks
+// (4 lanes), 128-element groups (16 lanes), static int8; token modes use s.
+template <int Q>
+__device__ __forceinline__ void encode_vec(const uint4& v, const float f[8], float s_token,
+                                           bool token_nonzero, uint32_t out[2], uint32_t& sbyte,
+                                           float& ginv) {
+    using TR = QTraits<Q>;
+    if constexpr (TR::token) {
+        encode_dynamic<Q>(f, s_token, token_nonzero, out);
+    } else if constexpr (TR::group) {
+        uint32_t m = absmax_bits8(f);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+        const float amax = __uint_as_float(m);
+        const float sg = __fdiv_rn(TR::dmax, amax);
+        ginv = __fdiv_rn(1.0f, sg);
+        encode_dynamic<Q>(f, sg, amax > 0.0f, out);
+    } else if constexpr (Q == M_INT8S) {
+        out[0] = q8s(f[0]) | (q8s(f[1]) << 8) | (q8s(f[2]) << 16) | (q8s(f[3]) << 24);
+        out[1] = q8s(f[4]) | (q8s(f[5]) << 8) | (q8s(f[6]) << 16) | (q8s(f[7]) << 24);
+    } else {
+        // MX: block b = vi / 4 lives in lanes 4m..4m+3 at the same u
+        uint32_t m = vec_absmax_bits(v);
+        m = max(m, __shfl_xor_sync(kFull, m, 1));
+        m = max(m, __shfl_xor_sync(kFull, m, 2));
+        const int ef = (int)(m >> 7) & 0xff;                 // bf16 exponent field
+        int se = (ef == 0) ? -127 : max(ef - 127 - TR::emax, -127);
+        se = min(se, 127);
+        sbyte = (uint32_t)(se + 127);
+        const float mul = __uint_as_float((uint32_t)(127 - se) << 23);  // 2^-se, exact
+        float g[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = __fmul_rn(f[i], mul);
+        if constexpr (Q == M_E2M1) {
+            out[0] = cvt_e2m1x8(g);
+            out[1] = 0;
+        } else {
+            out[0] = cvt_fp8x2<Q>(g[0], g[1]) | (cvt_fp8x2<Q>(g[2], g[3]) << 16);
+            out[1] = cvt_fp8x2<Q>(g[4], g[5]) | (cvt_fp8x2<Q>(g[6], g[7]) << 16);
+        }
+    }
+}
+
+// Quantised rows.  BULK: the encoded row (and a scale row whose size is a
+// multiple of 16 bytes) is written once into one of two shared-memory stages
+// and thread 0 sends it to the K destination rows with cp.async.bulk stores
+// (one bulk group per token; a stage is rewritten only after wait_group.read
+// shows the group of two tokens earlier has read it).  Otherwise every thread
+// stores its codes to each destination itself.  Scales here are NONE, SCALAR
+// or PER_CHANNEL (one encoding per token).
 template <int Q, int VPT, bool BULK>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) {
+    using TR = QTraits<Q>;
     extern __shared__ __align__(128) uint8_t qstage[];
     __shared__ int sdst[kMaxTopk];
     __shared__ uint32_t sred[8];
@@ -142,69 +253,42 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
         if (tid < a.K) sdst[tid] = a.dst_row[w * a.K + tid];
         const uint16_t* xrow = a.x + w * a.H;
         uint4 v[VPT];
+        float f[VPT][8];
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
             v[u] = vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0);
+            unpack8(v[u], f[u]);
         }
-        if constexpr (Q == M_INT8) {
+        if constexpr (!TR::mx) apply_scales<VPT>(f, a.smooth, a.smooth_kind, NT, a.nvec);
+        if constexpr (TR::token) {
             uint32_t m = 0;
 #pragma unroll
-            for (int u = 0; u < VPT; ++u) m = max(m, vec_absmax_bits(v[u]));
+            for (int u = 0; u < VPT; ++u) m = max(m, absmax_bits8(f[u]));
             for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
             if (lane == 0) sred[warp] = m;
         }
         __syncthreads();
 
-        // encode: code words per vector (8 bytes for int8 / fp8, 4 for e2m1)
-        uint32_t packed[VPT][2];
-        uint32_t sbyte[VPT];
-        float inv = 0.0f;
-        if constexpr (Q == M_INT8) {
+        float s_tok = 0.0f, inv = 0.0f, amax = 0.0f;
+        if constexpr (TR::token) {
             uint32_t m = 0;
             for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i]);
-            const float amax = bf16_bits_to_float(m);
-            const float s = __fdiv_rn(127.0f, amax);      // +inf for an all-zero row
-            inv = __fdiv_rn(1.0f, s);                      // 0 for an all-zero row
-#pragma unroll
-            for (int u = 0; u < VPT; ++u) {
-                float f[8];
-                unpack8(v[u], f);
-                sbyte[u] = 0;
-                if (amax > 0.0f) {
-                    packed[u][0] = q8(f[0], s) | (q8(f[1], s) << 8) | (q8(f[2], s) << 16) | (q8(f[3], s) << 24);
-                    packed[u][1] = q8(f[4], s) | (q8(f[5], s) << 8) | (q8(f[6], s) << 16) | (q8(f[7], s) << 24);
-                } else {
-                    packed[u][0] = packed[u][1] = 0;
-                }
-            }
-        } else {
-            // MX: block b = vi / 4 lives in lanes 4m..4m+3 at the same u
-            constexpr int emax = MxTraits<Q>::emax;
-#pragma unroll
-            for (int u = 0; u < VPT; ++u) {
-                uint32_t m = vec_absmax_bits(v[u]);
-                m = max(m, __shfl_xor_sync(kFull, m, 1));
-                m = max(m, __shfl_xor_sync(kFull, m, 2));
-                const int ef = (int)(m >> 7) & 0xff;                 // bf16 exponent field
-                int se = (ef == 0) ? -127 : max(ef - 127 - emax, -127);
-                se = min(se, 127);
-                sbyte[u] = (uint32_t)(se + 127);
-                const float mul = __uint_as_float((uint32_t)(127 - se) << 23);  // 2^-se, exact
-                float f[8];
-                unpack8(v[u], f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], mul);
-                if constexpr (Q == M_E2M1) {
-                    packed[u][0] = cvt_e2m1x8(f);
-                    packed[u][1] = 0;
-                } else {
-                    packed[u][0] = cvt_fp8x2<Q>(f[0], f[1]) | (cvt_fp8x2<Q>(f[2], f[3]) << 16);
-                    packed[u][1] = cvt_fp8x2<Q>(f[4], f[5]) | (cvt_fp8x2<Q>(f[6], f[7]) << 16);
-                }
-            }
+            amax = __uint_as_float(m);
+            s_tok = __fdiv_rn(TR::dmax, amax);   // +inf for an all-zero row
+            inv = __fdiv_rn(1.0f, s_tok);        // 0 for an all-zero row
         }
-        constexpr int VB = (Q == M_E2M1) ? 4 : 8;  // code bytes per 16-byte source vector
+        uint32_t packed[VPT][2];
+        uint32_t sbyte[VPT];
+        float ginv[VPT];
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            sbyte[u] = 0;
+            ginv[u] = 0.0f;
+            encode_vec<Q>(v[u], f[u], s_tok, amax > 0.0f, packed[u], sbyte[u], ginv[u]);
+        }
+        constexpr int VB = TR::VB;
+        const bool stage_scales = BULK && scale_bulk;
 
         if constexpr (BULK) {
             uint8_t* stg = qstage + (size_t)(j & 1) * stage_bytes;
@@ -214,7 +298,12 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
                 if (vi < a.nvec) {
                     if constexpr (VB == 4) *reinterpret_cast<uint32_t*>(stg + vi * 4) = packed[u][0];
                     else *reinterpret_cast<uint2*>(stg + vi * 8) = make_uint2(packed[u][0], packed[u][1]);
-                    if (Q != M_INT8 && scale_bulk && (vi & 3) == 0) stg[scale_off + (vi >> 2)] = (uint8_t)sbyte[u];
+                    if constexpr (TR::mx) {
+                        if (stage_scales && (vi & 3) == 0) stg[scale_off + (vi >> 2)] = (uint8_t)sbyte[u];
+                    } else if constexpr (TR::group) {
+                        if (stage_scales && (vi & 15) == 0)
+                            *reinterpret_cast<float*>(stg + scale_off + (vi >> 4) * 4) = ginv[u];
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -224,7 +313,7 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
                     const int d = sdst[k];
                     if (d < 0) continue;
                     bulk_store(a.data + (int64_t)d * a.row_bytes, stg, (uint32_t)a.row_bytes);
-                    if (Q != M_INT8 && scale_bulk)
+                    if (stage_scales)
                         bulk_store(a.scales + (int64_t)d * a.scale_bytes, stg + scale_off,
                                    (uint32_t)a.scale_bytes);
                 }
@@ -234,15 +323,20 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
         for (int k = 0; k < a.K; ++k) {
             const int d = sdst[k];
             if (d < 0) continue;
-            if constexpr (Q == M_INT8) {
+            if constexpr (TR::token) {
                 if (tid == 0) reinterpret_cast<float*>(a.scales)[d] = inv;
-            } else {
-                if (!(BULK && scale_bulk)) {
+            } else if constexpr (TR::mx || TR::group) {
+                if (!stage_scales) {
                     uint8_t* srow = a.scales + (int64_t)d * a.scale_bytes;
 #pragma unroll
                     for (int u = 0; u < VPT; ++u) {
                         const int vi = u * NT + tid;
-                        if (vi < a.nvec && (vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
+                        if (vi >= a.nvec) continue;
+                        if constexpr (TR::mx) {
+                            if ((vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
+                        } else {
+                            if ((vi & 15) == 0) reinterpret_cast<float*>(srow)[vi >> 4] = ginv[u];
+                        }
                     }
                 }
             }
@@ -262,6 +356,93 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
     }
     if constexpr (BULK) {
         if (tid == 0) bulk_wait_all();
+    }
+}
+
+// Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
+// encoded once per destination with the scale row of that destination's
+// expert (found from the row by bisection over expert_base); codes are stored
+// by every thread directly.
+template <int Q, int VPT>
+__global__ void __launch_bounds__(256)
+dispatch_expert_scaled_kernel(DispatchArgs a) {
+    using TR = QTraits<Q>;
+    extern __shared__ int sbase[];   // [E+1] first row of each expert
+    __shared__ int sdst[kMaxTopk];
+    __shared__ uint32_t sred[8];
+    const int total = a.expert_base[a.E];
+    if ((int64_t)total > a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
+        return;
+    }
+    const int NT = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
+    const int64_t items = a.N + a.E;
+    for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
+        if (w >= a.N) {
+            const int e = (int)(w - a.N);
+            const int64_t r0 = (int64_t)a.expert_base[e] + a.recv_cnt[e];
+            const int64_t r1 = a.expert_base[e + 1];
+            zero_rows(a, r0, r1);
+            continue;
+        }
+        __syncthreads();
+        if (tid < a.K) sdst[tid] = a.dst_row[w * a.K + tid];
+        const uint16_t* xrow = a.x + w * a.H;
+        uint4 v[VPT];
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * NT + tid;
+            v[u] = vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();
+        for (int k = 0; k < a.K; ++k) {
+            const int d = sdst[k];
+            if (d < 0) continue;
+            int lo = 0, hi = a.E;   // last expert e with sbase[e] <= d
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sbase[mid] <= d) lo = mid; else hi = mid;
+            }
+            float f[VPT][8];
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) unpack8(v[u], f[u]);
+            apply_scales<VPT>(f, a.smooth + (int64_t)lo * a.H, EP_SCALES_PER_CHANNEL, NT, a.nvec);
+            float s_tok = 0.0f, inv = 0.0f, amax = 0.0f;
+            if constexpr (TR::token) {
+                uint32_t m = 0;
+#pragma unroll
+                for (int u = 0; u < VPT; ++u) m = max(m, absmax_bits8(f[u]));
+                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+                if (lane == 0) sred[warp] = m;
+                __syncthreads();
+                m = 0;
+                for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i]);
+                __syncthreads();   // sred is rewritten for the next destination
+                amax = __uint_as_float(m);
+                s_tok = __fdiv_rn(TR::dmax, amax);
+                inv = __fdiv_rn(1.0f, s_tok);
+            }
+            uint8_t* row = a.data + (int64_t)d * a.row_bytes;
+            uint8_t* srow = a.scales ? a.scales + (int64_t)d * a.scale_bytes : nullptr;
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                uint32_t packed[2], sb = 0;
+                float gi = 0.0f;
+                encode_vec<Q>(v[u], f[u], s_tok, amax > 0.0f, packed, sb, gi);
+                const int vi = u * NT + tid;
+                if (vi < a.nvec) {
+                    st_v2(row + (int64_t)vi * 8, make_uint2(packed[0], packed[1]));
+                    if constexpr (TR::group) {
+                        if ((vi & 15) == 0) reinterpret_cast<float*>(srow)[vi >> 4] = gi;
+                    }
+                }
+            }
+            if constexpr (TR::token) {
+                if (tid == 0) reinterpret_cast<float*>(srow)[0] = inv;
+            }
+        }
     }
 }
 
@@ -393,10 +574,27 @@ template <int Q>
 cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     constexpr int VPT = 4;
     const int nt = ((a.nvec + VPT - 1) / VPT + 31) / 32 * 32;
+    if (a.smooth_kind == EP_SCALES_PER_EXPERT) {
+        if constexpr (QTraits<Q>::mx) {
+            return cudaErrorInvalidValue;
+        } else {
+            const size_t smem = sizeof(int) * (size_t)(a.E + 1);
+            int occ = 0;
+            cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &occ, dispatch_expert_scaled_kernel<Q, VPT>, nt, smem);
+            if (err != cudaSuccess) return err;
+            const int64_t items = a.N + a.E;
+            int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
+            if (grid > items) grid = items;
+            if (grid < 1) grid = 1;
+            dispatch_expert_scaled_kernel<Q, VPT><<<(unsigned)grid, nt, smem, st>>>(a);
+            return cudaGetLastError();
+        }
+    }
     // bulk stores need 16-byte rows (the receive buffer itself is 16-byte aligned)
     const bool bulk = (a.row_bytes % 16) == 0;
     if (!bulk) return launch_q_impl<Q, false>(h, a, nt, 0, 0, 0, st);
-    const int scale_bulk = (Q != M_INT8 && a.scale_bytes % 16 == 0 &&
+    const int scale_bulk = ((QTraits<Q>::mx || QTraits<Q>::group) && a.scale_bytes % 16 == 0 &&
                             ((uintptr_t)a.scales % 16) == 0) ? 1 : 0;
     const int scale_off = (a.row_bytes + 15) / 16 * 16;
     int stage_bytes = scale_off + (scale_bulk ? (a.scale_bytes + 15) / 16 * 16 : 0);
@@ -409,10 +607,15 @@ cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st)
 cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
     switch (quant) {
         case M_NONE: return launch_bf16_tma(h, a, st);
+        case M_INT8S: return launch_q<M_INT8S>(h, a, st);
         case M_INT8: return launch_q<M_INT8>(h, a, st);
         case M_E4M3: return launch_q<M_E4M3>(h, a, st);
         case M_E5M2: return launch_q<M_E5M2>(h, a, st);
         case M_E2M1: return launch_q<M_E2M1>(h, a, st);
+        case M_FP8T_E4M3: return launch_q<M_FP8T_E4M3>(h, a, st);
+        case M_FP8T_E5M2: return launch_q<M_FP8T_E5M2>(h, a, st);
+        case M_FP8G_E4M3: return launch_q<M_FP8G_E4M3>(h, a, st);
+        case M_FP8G_E5M2: return launch_q<M_FP8G_E5M2>(h, a, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -15,9 +15,15 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 bool is_mx(int q) { return q == EP_QUANT_MXFP8_E4M3 || q == EP_QUANT_MXFP8_E5M2 || q == EP_QUANT_MXFP4_E2M1; }
 
+bool is_group(int q) { return q == EP_QUANT_FP8_E4M3_PER_GROUP || q == EP_QUANT_FP8_E5M2_PER_GROUP; }
+
 bool valid_quant(int q) {
-    return q == EP_QUANT_NONE || q == EP_QUANT_INT8_PER_TOKEN || is_mx(q);
+    return q == EP_QUANT_NONE || q == EP_QUANT_INT8_STATIC || q == EP_QUANT_INT8_PER_TOKEN || is_mx(q) ||
+           q == EP_QUANT_FP8_E4M3_PER_TOKEN || q == EP_QUANT_FP8_E5M2_PER_TOKEN || is_group(q);
 }
+
+// quantModes 1-3 take input scales; NONE and MX take none
+bool takes_scales(int q) { return q != EP_QUANT_NONE && !is_mx(q); }
 
 struct Tiling { int32_t C, TPB, B; };
 
@@ -136,12 +142,18 @@ ep_status ep_recv_row_bytes(int32_t hidden, ep_quant_mode q, int64_t* data_bytes
     if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
     if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
     if (is_mx(q) && hidden % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (is_group(q) && hidden % 128 != 0) return EP_ERR_INVALID_ARG;
     switch (q) {
         case EP_QUANT_NONE: *data_bytes = 2 * (int64_t)hidden; *scale_bytes = 0; break;
-        case EP_QUANT_INT8_PER_TOKEN: *data_bytes = hidden; *scale_bytes = 4; break;
+        case EP_QUANT_INT8_STATIC: *data_bytes = hidden; *scale_bytes = 0; break;
+        case EP_QUANT_INT8_PER_TOKEN:
+        case EP_QUANT_FP8_E4M3_PER_TOKEN:
+        case EP_QUANT_FP8_E5M2_PER_TOKEN: *data_bytes = hidden; *scale_bytes = 4; break;
         case EP_QUANT_MXFP8_E4M3:
         case EP_QUANT_MXFP8_E5M2: *data_bytes = hidden; *scale_bytes = hidden / 32; break;
         case EP_QUANT_MXFP4_E2M1: *data_bytes = hidden / 2; *scale_bytes = hidden / 32; break;
+        case EP_QUANT_FP8_E4M3_PER_GROUP:
+        case EP_QUANT_FP8_E5M2_PER_GROUP: *data_bytes = hidden; *scale_bytes = 4 * (hidden / 128); break;
     }
     return EP_OK;
 }
@@ -189,10 +201,16 @@ ep_status ep_handle_destroy(ep_handle* h) {
 }
 
 ep_status ep_layout(ep_handle* h, const int64_t* topk, ep_stream_t stream) {
+    return ep_layout_masked(h, topk, nullptr, 0, stream);
+}
+
+ep_status ep_layout_masked(ep_handle* h, const int64_t* topk, const uint8_t* mask, int32_t mask_dims,
+                           ep_stream_t stream) {
     if (!h) return EP_ERR_INVALID_ARG;
     if (h->N > 0 && (!topk || !aligned_to(topk, 8))) return EP_ERR_INVALID_ARG;
+    if (mask && mask_dims != 1 && mask_dims != 2) return EP_ERR_INVALID_ARG;
     if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
-    return from_cuda(launch_layout(h, topk, (cudaStream_t)stream));
+    return from_cuda(launch_layout(h, topk, mask, mask ? mask_dims : 0, (cudaStream_t)stream));
 }
 
 ep_status ep_handle_views(const ep_handle* h, ep_layout_views* v) {
@@ -241,22 +259,35 @@ ep_status ep_handle_status(const ep_handle* h, ep_stream_t stream) {
 
 ep_status ep_dispatch(const ep_handle* hc, const void* x, ep_quant_mode q, void* recv_data,
                       void* recv_scales, int64_t cap, ep_stream_t stream) {
+    return ep_dispatch_scaled(hc, x, q, nullptr, EP_SCALES_NONE, recv_data, recv_scales, cap, stream);
+}
+
+ep_status ep_dispatch_scaled(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
+                             ep_scale_kind kind, void* recv_data, void* recv_scales, int64_t cap,
+                             ep_stream_t stream) {
     ep_handle* h = const_cast<ep_handle*>(hc);
     if (!h) return EP_ERR_INVALID_ARG;
     if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
     if (is_mx(q) && h->H % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (is_group(q) && h->H % 128 != 0) return EP_ERR_INVALID_ARG;
+    if (kind < EP_SCALES_NONE || kind > EP_SCALES_PER_EXPERT) return EP_ERR_INVALID_ARG;
+    if (kind != EP_SCALES_NONE && !takes_scales(q)) return EP_ERR_INVALID_ARG;
+    if (q == EP_QUANT_INT8_STATIC && kind == EP_SCALES_NONE) return EP_ERR_INVALID_ARG;
+    if (kind != EP_SCALES_NONE && (!scales || !aligned_to(scales, kind == EP_SCALES_SCALAR ? 4 : 16)))
+        return EP_ERR_INVALID_ARG;
     if (cap < 0) return EP_ERR_INVALID_ARG;
     if (h->N > 0 && (!x || !aligned_to(x, 16))) return EP_ERR_INVALID_ARG;
     if (!recv_data && cap > 0) return EP_ERR_INVALID_ARG;
     if (recv_data && !aligned_to(recv_data, 16)) return EP_ERR_INVALID_ARG;
-    if (q != EP_QUANT_NONE && cap > 0 && (!recv_scales || !aligned_to(recv_scales, 4)))
-        return EP_ERR_INVALID_ARG;
-    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
     int64_t db = 0, sb = 0;
     ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);
     if (s != EP_OK) return s;
+    if (sb > 0 && cap > 0 && (!recv_scales || !aligned_to(recv_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
     DispatchArgs a;
     a.x = (const uint16_t*)x;
+    a.smooth = scales;
+    a.smooth_kind = (int32_t)kind;
     a.data = (uint8_t*)recv_data;
     a.scales = (uint8_t*)recv_scales;
     a.dst_row = h->dst_row;
@@ -303,9 +334,10 @@ ep_status ep_expert_identity(const ep_handle* hc, ep_quant_mode q, const void* r
     if (!h) return EP_ERR_INVALID_ARG;
     if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
     if (is_mx(q) && h->H % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (is_group(q) && h->H % 128 != 0) return EP_ERR_INVALID_ARG;
     if (cap < 0 || mark_mod < 0) return EP_ERR_INVALID_ARG;
     if (cap > 0 && (!recv_data || !y || !aligned_to(y, 4))) return EP_ERR_INVALID_ARG;
-    if (q != EP_QUANT_NONE && cap > 0 && !recv_scales) return EP_ERR_INVALID_ARG;
+    if (q != EP_QUANT_NONE && q != EP_QUANT_INT8_STATIC && cap > 0 && !recv_scales) return EP_ERR_INVALID_ARG;
     if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
     int64_t db = 0, sb = 0;
     ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);

@@ -54,6 +54,8 @@ struct ep_handle {
 // Argument block shared by the three layout kernels.
 struct LayoutArgs {
     const int64_t* topk;
+    const uint8_t* mask;      // xActiveMask or null
+    int32_t mask_dims;        // 1: [N] per token, 2: [N*K] per entry
     int32_t R, T, E, K, L, alpha, C, TPB, B;
     int64_t recv_cap;
     int32_t* status;
@@ -76,6 +78,8 @@ struct LayoutArgs {
 
 struct DispatchArgs {
     const uint16_t* x;        // [N][H] bf16
+    const float* smooth;      // input scales of quantModes 1-3, or null
+    int32_t smooth_kind;      // ep_scale_kind
     uint8_t* data;            // [cap][row_bytes]
     uint8_t* scales;          // [cap][scale_bytes] or null
     const int32_t* dst_row;   // [N][K]
@@ -114,7 +118,8 @@ struct IdentityArgs {
 };
 
 // Launchers (return cudaGetLastError() after the launch).
-cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, cudaStream_t st);
+cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t* mask,
+                          int mask_dims, cudaStream_t st);
 cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st);
 cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant, cudaStream_t st);

@@ -1,6 +1,7 @@
 // layout.cu -- routing layout from topk_idx (DeepEP "Normal Mode API" layout
-// inputs; CANN aclnnMoeDistributeDispatchV2 expert placement; MAX
-// EPBatchManager.ep_dispatch expert_start_indices / expert_usage_stats).
+// inputs; CANN aclnnMoeDistributeDispatchV2 expert placement and
+// xActiveMask; MAX EPBatchManager.ep_dispatch expert_start_indices /
+// expert_usage_stats).
 //
 // Three kernels, no inter-CTA waiting:
 //   count  - per CTA (a contiguous token range of one source rank): expert
@@ -22,6 +23,16 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Expert id of entry i; an entry masked out by xActiveMask reads as -1.
+__device__ __forceinline__ int64_t entry_expert(const LayoutArgs& a, int64_t i) {
+    const int64_t e = a.topk[i];
+    if (a.mask) {
+        const uint8_t act = a.mask_dims == 1 ? a.mask[i / a.K] : a.mask[i];
+        if (!act) return -1;
+    }
+    return e;
+}
+
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_count_kernel(LayoutArgs a) {
     extern __shared__ int smem[];
@@ -39,7 +50,7 @@ layout_count_kernel(LayoutArgs a) {
     if (t1 > t0) {
         const int64_t ebeg = (n0 + t0) * a.K, eend = (n0 + t1) * a.K;
         for (int64_t i = ebeg + threadIdx.x; i < eend; i += blockDim.x) {
-            const int64_t e = a.topk[i];
+            const int64_t e = entry_expert(a, i);
             if (e == -1) continue;
             if (e < -1 || e >= a.E) { bad = true; continue; }
             atomicAdd(&hist[(int)e], 1);
@@ -51,7 +62,7 @@ layout_count_kernel(LayoutArgs a) {
             const int64_t n = n0 + t;
             int rk = -1;
             if (lane < a.K) {
-                const int64_t e = a.topk[n * a.K + lane];
+                const int64_t e = entry_expert(a, n * a.K + lane);
                 if (e >= 0 && e < a.E) rk = (int)e / a.L;
             }
             for (int j0 = 0; j0 < a.R; j0 += 32) {
@@ -213,7 +224,7 @@ layout_assign_kernel(LayoutArgs a) {
     for (int e = lane; e < E; e += 32) mycnt[e] = 0;
     __syncwarp();
     for (int i = w0 + lane; i < w1; i += 32) {
-        const int64_t e = a.topk[ebeg + i];
+        const int64_t e = entry_expert(a, ebeg + i);
         if (e >= 0 && e < E) atomicAdd(&mycnt[(int)e], 1);
     }
     __syncthreads();
@@ -233,7 +244,7 @@ layout_assign_kernel(LayoutArgs a) {
         const int i = i0 + lane;
         int e = -1;
         if (i < w1) {
-            const int64_t ev = a.topk[ebeg + i];
+            const int64_t ev = entry_expert(a, ebeg + i);
             if (ev >= 0 && ev < E) e = (int)ev;
         }
         const unsigned peers = __match_any_sync(kFull, e);
@@ -251,9 +262,12 @@ layout_assign_kernel(LayoutArgs a) {
 
 }  // namespace
 
-cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, cudaStream_t st) {
+cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t* mask,
+                          int mask_dims, cudaStream_t st) {
     LayoutArgs a;
     a.topk = topk;
+    a.mask = mask;
+    a.mask_dims = mask_dims;
     a.R = h->R; a.T = h->T; a.E = h->E; a.K = h->K; a.L = h->L; a.alpha = h->alpha;
     a.C = h->C; a.TPB = h->TPB; a.B = h->B;
     a.recv_cap = h->recv_cap;

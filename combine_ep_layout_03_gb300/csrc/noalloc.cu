@@ -122,5 +122,5 @@ extern "C" ep_status ep_layout_static_scratch(const ep_params* p, const int64_t*
     h.recv_src = o->recv_src;
     h.expert_ids = o->expert_ids;
     h.usage = o->expert_usage_stats;
-    return launch_layout(&h, topk, (cudaStream_t)stream) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return launch_layout(&h, topk, nullptr, 0, (cudaStream_t)stream) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }

@@ -20,12 +20,20 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CAPACITY = 0, 1, 2, 3
 EP_ERR_BAD_EXPERT_ID, EP_ERR_TIMEOUT, EP_ERR_CUDA = 4, 5, 6
 
 EP_QUANT_NONE = 0
+EP_QUANT_INT8_STATIC = 1
 EP_QUANT_INT8_PER_TOKEN = 2
 EP_QUANT_MXFP8_E4M3 = 4
 EP_QUANT_MXFP8_E5M2 = 5
 EP_QUANT_MXFP4_E2M1 = 6
-QUANT_MODES = (EP_QUANT_NONE, EP_QUANT_INT8_PER_TOKEN, EP_QUANT_MXFP8_E4M3,
-               EP_QUANT_MXFP8_E5M2, EP_QUANT_MXFP4_E2M1)
+EP_QUANT_FP8_E4M3_PER_TOKEN = 7
+EP_QUANT_FP8_E5M2_PER_TOKEN = 8
+EP_QUANT_FP8_E4M3_PER_GROUP = 9
+EP_QUANT_FP8_E5M2_PER_GROUP = 10
+QUANT_MODES = (EP_QUANT_NONE, EP_QUANT_INT8_STATIC, EP_QUANT_INT8_PER_TOKEN, EP_QUANT_MXFP8_E4M3,
+               EP_QUANT_MXFP8_E5M2, EP_QUANT_MXFP4_E2M1, EP_QUANT_FP8_E4M3_PER_TOKEN,
+               EP_QUANT_FP8_E5M2_PER_TOKEN, EP_QUANT_FP8_E4M3_PER_GROUP, EP_QUANT_FP8_E5M2_PER_GROUP)
+
+EP_SCALES_NONE, EP_SCALES_SCALAR, EP_SCALES_PER_CHANNEL, EP_SCALES_PER_EXPERT = 0, 1, 2, 3
 
 
 class EPError(RuntimeError):
@@ -70,11 +78,13 @@ def _load():
         "ep_handle_create": ([P, vp, ctypes.c_size_t, ctypes.POINTER(vp)], st),
         "ep_handle_destroy": ([vp], st),
         "ep_layout": ([vp, vp, vp], st),
+        "ep_layout_masked": ([vp, vp, vp, i32, vp], st),
         "ep_handle_views": ([vp, ctypes.POINTER(ep_layout_views)], st),
         "ep_handle_recv_rows": ([vp, vp, vp], st),
         "ep_handle_expert_counts": ([vp, vp, vp], st),
         "ep_handle_status": ([vp, vp], st),
         "ep_dispatch": ([vp, vp, st, vp, vp, i64, vp], st),
+        "ep_dispatch_scaled": ([vp, vp, st, vp, st, vp, vp, i64, vp], st),
         "ep_combine": ([vp, vp, i64, vp, vp, i32, vp, vp], st),
         "ep_expert_identity": ([vp, st, vp, vp, i64, i32, vp, vp], st),
         "ep_layout_static_scratch": ([P, vp, ctypes.POINTER(ep_layout_outputs), vp], st),
@@ -152,6 +162,11 @@ def ep_layout(h: int, topk_idx: torch.Tensor, stream=None) -> None:
     _check(_lib.ep_layout(h, _ptr(topk_idx), _stream(stream)), "ep_layout")
 
 
+def ep_layout_masked(h: int, topk_idx: torch.Tensor, mask, mask_dims: int, stream=None) -> None:
+    _check(_lib.ep_layout_masked(h, _ptr(topk_idx), _ptr(mask), int(mask_dims), _stream(stream)),
+           "ep_layout_masked")
+
+
 def ep_handle_views(h: int) -> ep_layout_views:
     v = ep_layout_views()
     _check(_lib.ep_handle_views(h, ctypes.byref(v)), "ep_handle_views")
@@ -179,6 +194,13 @@ def ep_dispatch(h: int, x, quant: int, recv_data, recv_scales, recv_rows_capacit
                 stream=None) -> None:
     _check(_lib.ep_dispatch(h, _ptr(x), quant, _ptr(recv_data), _ptr(recv_scales),
                             int(recv_rows_capacity), _stream(stream)), "ep_dispatch")
+
+
+def ep_dispatch_scaled(h: int, x, quant: int, scales, scale_kind: int, recv_data, recv_scales,
+                       recv_rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_dispatch_scaled(h, _ptr(x), quant, _ptr(scales), int(scale_kind), _ptr(recv_data),
+                                   _ptr(recv_scales), int(recv_rows_capacity), _stream(stream)),
+           "ep_dispatch_scaled")
 
 
 def ep_combine(h: int, y, y_rows_capacity: int, topk_weights, shared, num_shared: int, out,
@@ -242,10 +264,19 @@ class EPLayout:
     def worst_rows(self) -> int:
         return self.R * self.T * self.K + self.E * (self.alpha - 1)
 
-    def layout(self, topk_idx: torch.Tensor, stream=None) -> "EPLayout":
+    def layout(self, topk_idx: torch.Tensor, stream=None, active_mask: torch.Tensor | None = None
+               ) -> "EPLayout":
+        """active_mask (xActiveMask): uint8/bool [R, T] per token or [R, T, K] per entry."""
         assert topk_idx.dtype == torch.int64 and topk_idx.is_contiguous()
         assert topk_idx.numel() == self.R * self.T * self.K
-        ep_layout(self.h, topk_idx, stream)
+        if active_mask is None:
+            ep_layout(self.h, topk_idx, stream)
+        else:
+            m = active_mask.to(torch.uint8).contiguous()
+            dims = 1 if m.numel() == self.R * self.T else 2
+            assert m.numel() == (self.R * self.T if dims == 1 else self.R * self.T * self.K)
+            self._mask = m  # keep alive until the kernels ran
+            ep_layout_masked(self.h, topk_idx, m, dims, stream)
         return self
 
     def views(self) -> dict[str, torch.Tensor]:
@@ -280,10 +311,14 @@ class EPLayout:
         return data, scales
 
     def dispatch(self, x: torch.Tensor, quant: int, recv_data: torch.Tensor,
-                 recv_scales: torch.Tensor | None, stream=None) -> None:
+                 recv_scales: torch.Tensor | None, stream=None, scales: torch.Tensor | None = None,
+                 scale_kind: int = EP_SCALES_NONE) -> None:
         db, _ = ep_recv_row_bytes(self.H, quant)
         cap = recv_data.numel() // db
-        ep_dispatch(self.h, x, quant, recv_data, recv_scales, cap, stream)
+        if scales is None and scale_kind == EP_SCALES_NONE:
+            ep_dispatch(self.h, x, quant, recv_data, recv_scales, cap, stream)
+        else:
+            ep_dispatch_scaled(self.h, x, quant, scales, scale_kind, recv_data, recv_scales, cap, stream)
 
     def combine(self, y: torch.Tensor, topk_weights: torch.Tensor, out: torch.Tensor,
                 shared: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -36,7 +36,8 @@ from dataclasses import dataclass, replace
 import numpy as np
 import torch
 
-QUANT_NAMES = {0: "none", 2: "int8", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2", 6: "mxfp4_e2m1"}
+QUANT_NAMES = {0: "none", 1: "int8_static", 2: "int8", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2", 6: "mxfp4_e2m1",
+               7: "fp8_e4m3_token", 8: "fp8_e5m2_token", 9: "fp8_e4m3_group128", 10: "fp8_e5m2_group128"}
 
 
 @dataclass(frozen=True)
@@ -202,3 +203,20 @@ def gen_shared_device(w: Workload, device="cuda") -> torch.Tensor | None:
         b = min(flat.shape[0], a + step)
         flat[a:b] = torch.randn((b - a, w.H), generator=g, device=device).to(torch.bfloat16)
     return out
+
+
+def gen_scales(w: Workload, kind: int, stream: int = 7) -> np.ndarray | None:
+    """Input scales of quantModes 1-3: kind 1 -> [1], 2 -> [H], 3 -> [E, H];
+    float32 uniform in [0.5, 2) (a smooth weight around 1).  kind 0 -> None."""
+    if kind == 0:
+        return None
+    rng = _rng(w, stream)
+    shape = {1: (1,), 2: (w.H,), 3: (w.E, w.H)}[kind]
+    return (0.5 + 1.5 * rng.random(shape)).astype(np.float32)
+
+
+def gen_mask(w: Workload, dims: int, p_active: float = 0.9, stream: int = 8) -> np.ndarray:
+    """xActiveMask: uint8 [R, T] (dims 1) or [R, T, K] (dims 2), Bernoulli(p_active)."""
+    rng = _rng(w, stream)
+    shape = (w.R, w.T) if dims == 1 else (w.R, w.T, w.K)
+    return (rng.random(shape) < p_active).astype(np.uint8)

@@ -63,15 +63,31 @@ typedef enum ep_status {
     EP_ERR_CUDA = 6           /* a CUDA runtime call or kernel launch failed */
 } ep_status;
 
-/* Receive-row encodings (CANN quantMode numbering for 0 and 2; the MX variants
- * of quantMode 4 are split by element type). */
+/* Receive-row encodings (CANN quantMode numbering for 0, 1 and 2; the MX
+ * variants of quantMode 4 and the FP8 destinations of quantModes 2 and 3 are
+ * split by element type). */
 typedef enum ep_quant_mode {
-    EP_QUANT_NONE = 0,           /* bf16 rows [rows, H] (quantMode 0) */
-    EP_QUANT_INT8_PER_TOKEN = 2, /* int8 [rows, H] + float32 inverse scale [rows] (quantMode 2) */
-    EP_QUANT_MXFP8_E4M3 = 4,     /* e4m3 [rows, H] + e8m0 [rows, H/32] (quantMode 4) */
-    EP_QUANT_MXFP8_E5M2 = 5,     /* e5m2 [rows, H] + e8m0 [rows, H/32] (quantMode 4) */
-    EP_QUANT_MXFP4_E2M1 = 6      /* e2m1 x2 [rows, H/2] + e8m0 [rows, H/32] */
+    EP_QUANT_NONE = 0,                 /* bf16 rows [rows, H] (quantMode 0) */
+    EP_QUANT_INT8_STATIC = 1,          /* int8 [rows, H], no scales sent (quantMode 1; needs input scales) */
+    EP_QUANT_INT8_PER_TOKEN = 2,       /* int8 [rows, H] + float32 inverse scale [rows] (quantMode 2) */
+    EP_QUANT_MXFP8_E4M3 = 4,           /* e4m3 [rows, H] + e8m0 [rows, H/32] (quantMode 4) */
+    EP_QUANT_MXFP8_E5M2 = 5,           /* e5m2 [rows, H] + e8m0 [rows, H/32] (quantMode 4) */
+    EP_QUANT_MXFP4_E2M1 = 6,           /* e2m1 x2 [rows, H/2] + e8m0 [rows, H/32] */
+    EP_QUANT_FP8_E4M3_PER_TOKEN = 7,   /* e4m3 [rows, H] + float32 inverse scale [rows] (quantMode 2) */
+    EP_QUANT_FP8_E5M2_PER_TOKEN = 8,   /* e5m2 [rows, H] + float32 inverse scale [rows] (quantMode 2) */
+    EP_QUANT_FP8_E4M3_PER_GROUP = 9,   /* e4m3 [rows, H] + float32 [rows, H/128] (quantMode 3) */
+    EP_QUANT_FP8_E5M2_PER_GROUP = 10   /* e5m2 [rows, H] + float32 [rows, H/128] (quantMode 3) */
 } ep_quant_mode;
+
+/* Input scales of quantModes 1-3 (CANN: "scales" of shape (1,), (H,) --
+ * a smooth weight shared by every expert -- or (E, H), one row per expert):
+ * the row is multiplied element-wise by the scales before quantisation. */
+typedef enum ep_scale_kind {
+    EP_SCALES_NONE = 0,
+    EP_SCALES_SCALAR = 1,      /* float32 [1] */
+    EP_SCALES_PER_CHANNEL = 2, /* float32 [H] */
+    EP_SCALES_PER_EXPERT = 3   /* float32 [E, H]; each entry uses its expert's row */
+} ep_scale_kind;
 
 /* Problem description.  Constraints (checked by ep_params_validate):
  *   num_ranks R >= 1; num_experts E in [1, 512] with E % R == 0 (localExpertNum
@@ -135,8 +151,10 @@ ep_status ep_params_validate(const ep_params* params);
 ep_status ep_layout_workspace_size(const ep_params* params, size_t* bytes);
 
 /* Host only.  Bytes of one receive row's data part and scale part for a quant
- * mode and hidden size (bf16: 2H and 0; int8: H and 4; e4m3/e5m2: H and H/32;
- * e2m1: H/2 and H/32).  H must satisfy the mode's divisibility rule. */
+ * mode and hidden size (bf16: 2H and 0; static int8: H and 0; per-token int8 /
+ * FP8: H and 4; MX e4m3/e5m2: H and H/32; e2m1: H/2 and H/32; per-group FP8: H
+ * and 4*H/128).  H must satisfy the mode's divisibility rule (MX: H % 32 == 0;
+ * per-group: H % 128 == 0). */
 ep_status ep_recv_row_bytes(int32_t hidden, ep_quant_mode quant,
                             int64_t* data_bytes, int64_t* scale_bytes);
 
@@ -163,6 +181,14 @@ ep_status ep_handle_destroy(ep_handle* handle);
  * recv_capacity_rows sets EP_ERR_CAPACITY (recv_src then holds only the rows
  * that fit).  Three kernels, no host synchronisation. */
 ep_status ep_layout(ep_handle* handle, const int64_t* topk_idx, ep_stream_t stream);
+
+/* Device.  ep_layout with CANN's xActiveMask: active_mask is uint8 [R, T]
+ * (mask_dims = 1: a zero token takes no part in the communication) or
+ * [R, T, K] (mask_dims = 2: a zero entry takes no part); a masked entry is laid
+ * out exactly like a topk id of -1.  The page asks 1-D masks to be a prefix of
+ * true values; any pattern is accepted here.  NULL mask = ep_layout. */
+ep_status ep_layout_masked(ep_handle* handle, const int64_t* topk_idx, const uint8_t* active_mask,
+                           int32_t mask_dims, ep_stream_t stream);
 
 /* Host only.  Device pointers to the layout arrays (valid after ep_layout's
  * kernels have run on the stream). */
@@ -206,6 +232,23 @@ ep_status ep_dispatch(const ep_handle* handle, const void* x, ep_quant_mode quan
                       void* recv_data, void* recv_scales, int64_t recv_rows_capacity,
                       ep_stream_t stream);
 
+/* Device.  ep_dispatch for every quant mode, with CANN's optional input scales
+ * (quantModes 1-3): xFp32 = x * scales, element-wise, before the mode's rule.
+ *   INT8_STATIC (quantMode 1): code = round-half-even(xFp32) saturated to
+ *     [-128, 127]; no scale is sent; scales are required.
+ *   INT8_PER_TOKEN / FP8_*_PER_TOKEN (quantMode 2): s = dstTypeMax / max|xFp32|
+ *     over the row (127, 448, 57344), code = cast(xFp32 * s), scale word 1/s.
+ *   FP8_*_PER_GROUP (quantMode 3): the same rule per group of 128 elements,
+ *     one float32 1/s per group.
+ *   NONE and the MX modes take no scales (kind must be EP_SCALES_NONE).
+ * scales: device float32 of the kind's shape.  With EP_SCALES_PER_EXPERT a
+ * token is encoded separately for each destination with that expert's row.
+ * Layouts, capacity and errors as for ep_dispatch. */
+ep_status ep_dispatch_scaled(const ep_handle* handle, const void* x, ep_quant_mode quant,
+                             const float* scales, ep_scale_kind scale_kind,
+                             void* recv_data, void* recv_scales, int64_t recv_rows_capacity,
+                             ep_stream_t stream);
+
 /* Device.  Combine (DeepEP combine, MAX ep_combine): for every source token,
  *   out[s,t,:] = bf16( sum_k w[s,t,k] * y[dst_row[s,t,k],:]
  *                      + sum_{q<num_shared} shared[s,q,t,:] )
@@ -226,8 +269,11 @@ ep_status ep_combine(const ep_handle* handle, const void* y, int64_t y_rows_capa
  * combine): y[r,:] = bf16(dequant(recv row r) * 2^-(e(r) mod mark_mod)), where
  * e(r) is the row's expert, dequant is the bf16 value (NONE), q * scale
  * (INT8_PER_TOKEN) or code value * 2^sharedExp (MX), and mark_mod = 0 means
- * no mark.  Padding rows give zeros.  Shapes as in ep_dispatch; y is
- * [rows_capacity, H] bf16. */
+ * no mark.  Dequantisation: bf16 value (NONE); q * scale word (per-token int8
+ * and FP8; per-group FP8 with its group's word); code value * 2^sharedExp (MX);
+ * the integer code itself (static int8, whose scales the receiver holds).
+ * Padding rows give zeros.  Shapes as in ep_dispatch; y is [rows_capacity, H]
+ * bf16. */
 ep_status ep_expert_identity(const ep_handle* handle, ep_quant_mode quant,
                              const void* recv_data, const void* recv_scales,
                              int64_t rows_capacity, int32_t mark_mod, void* y,

@@ -147,7 +147,7 @@ def test_launching_calls_validate_before_touching_cuda():
     assert L.ep_combine(h, 1 << 40, 10, 1 << 42, None, 2, 1 << 41, None) == ep.EP_ERR_INVALID_ARG  # no shared
     assert L.ep_combine(h, 1 << 40, 10, 1 << 42, None, 0, (1 << 41) + 4, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_layout(h, None, None) == ep.EP_ERR_INVALID_ARG
-    assert L.ep_expert_identity(h, 9, 1 << 40, None, 4, 0, 1 << 41, None) == ep.EP_ERR_UNSUPPORTED
+    assert L.ep_expert_identity(h, 11, 1 << 40, None, 4, 0, 1 << 41, None) == ep.EP_ERR_UNSUPPORTED
     assert L.ep_expert_identity(h, 0, 1 << 40, None, 4, -1, 1 << 41, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_layout(None, None, None) == ep.EP_ERR_INVALID_ARG
     ep.ep_handle_destroy(h)
@@ -169,3 +169,36 @@ def test_combine_rejects_too_many_shared_rows():
     st, h, _ = _create_fake(p)
     assert ep.lib.ep_combine(h, 1 << 40, 10, 1 << 42, 1 << 43, 17, 1 << 41, None) == ep.EP_ERR_INVALID_ARG
     ep.ep_handle_destroy(h)
+
+
+def test_scaled_dispatch_and_mask_validation():
+    p = ep.make_params(2, 8, 256, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C = 1 << 40, 1 << 41, 1 << 42
+    # static int8 needs scales; MX and bf16 take none; unknown kind; unaligned per-channel scales
+    assert L.ep_dispatch_scaled(h, A, 1, None, 0, B, None, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch_scaled(h, A, 4, C, 2, B, C, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch_scaled(h, A, 0, C, 1, B, None, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch_scaled(h, A, 2, C, 7, B, C, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch_scaled(h, A, 2, C + 4, 2, B, C, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch_scaled(h, A, 9, None, 0, B, None, 10, None) == ep.EP_ERR_INVALID_ARG  # no scale buffer
+    assert L.ep_dispatch_scaled(h, A, 11, None, 0, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED
+    # mask dims must be 1 or 2
+    assert L.ep_layout_masked(h, A, B, 3, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
+    # per-group FP8 needs H % 128 == 0
+    p = ep.make_params(2, 8, 96, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    assert L.ep_dispatch_scaled(h, A, 9, None, 0, B, C, 10, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
+
+
+def test_row_bytes_new_modes():
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_INT8_STATIC) == (4096, 0)
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_FP8_E4M3_PER_TOKEN) == (4096, 4)
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_FP8_E5M2_PER_TOKEN) == (4096, 4)
+    assert ep.ep_recv_row_bytes(4096, ep.EP_QUANT_FP8_E4M3_PER_GROUP) == (4096, 128)
+    assert ep.ep_recv_row_bytes(7168, ep.EP_QUANT_FP8_E5M2_PER_GROUP) == (7168, 224)
+    with pytest.raises(ep.EPError):
+        ep.ep_recv_row_bytes(4160, ep.EP_QUANT_FP8_E4M3_PER_GROUP)
