@@ -361,15 +361,20 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
-// expert (found from the row by bisection over expert_base); codes are stored
-// by every thread directly.
+// expert.  Threads 0..K-1 find the K experts (bisection over expert_base);
+// each destination then takes one pass over its scale-row slice (per-token
+// modes add one CTA reduction of the row maximum; each destination has its
+// own reduction slot, so one barrier per destination suffices) and every
+// thread stores its codes directly.  The cost is dominated by reading K scale
+// rows of H floats per token from L2.
 template <int Q, int VPT>
 __global__ void __launch_bounds__(256)
 dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
     extern __shared__ int sbase[];   // [E+1] first row of each expert
     __shared__ int sdst[kMaxTopk];
-    __shared__ uint32_t sred[8];
+    __shared__ int sexp[kMaxTopk];
+    __shared__ uint32_t sred[8][kMaxTopk];
     const int total = a.expert_base[a.E];
     if ((int64_t)total > a.cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
@@ -378,6 +383,7 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
     const int NT = blockDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
+    __syncthreads();
     const int64_t items = a.N + a.E;
     for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
         if (w >= a.N) {
@@ -387,8 +393,20 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
             zero_rows(a, r0, r1);
             continue;
         }
-        __syncthreads();
-        if (tid < a.K) sdst[tid] = a.dst_row[w * a.K + tid];
+        __syncthreads();   // sdst / sexp / sred of the previous token are consumed
+        if (tid < a.K) {
+            const int d = a.dst_row[w * a.K + tid];
+            int lo = 0;
+            if (d >= 0) {
+                int hi = a.E;   // last expert e with sbase[e] <= d
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sbase[mid] <= d) lo = mid; else hi = mid;
+                }
+            }
+            sdst[tid] = d;
+            sexp[tid] = lo;
+        }
         const uint16_t* xrow = a.x + w * a.H;
         uint4 v[VPT];
 #pragma unroll
@@ -400,26 +418,20 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
         for (int k = 0; k < a.K; ++k) {
             const int d = sdst[k];
             if (d < 0) continue;
-            int lo = 0, hi = a.E;   // last expert e with sbase[e] <= d
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (sbase[mid] <= d) lo = mid; else hi = mid;
-            }
             float f[VPT][8];
 #pragma unroll
             for (int u = 0; u < VPT; ++u) unpack8(v[u], f[u]);
-            apply_scales<VPT>(f, a.smooth + (int64_t)lo * a.H, EP_SCALES_PER_CHANNEL, NT, a.nvec);
+            apply_scales<VPT>(f, a.smooth + (int64_t)sexp[k] * a.H, EP_SCALES_PER_CHANNEL, NT, a.nvec);
             float s_tok = 0.0f, inv = 0.0f, amax = 0.0f;
             if constexpr (TR::token) {
                 uint32_t m = 0;
 #pragma unroll
                 for (int u = 0; u < VPT; ++u) m = max(m, absmax_bits8(f[u]));
                 for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
-                if (lane == 0) sred[warp] = m;
+                if (lane == 0) sred[warp][k] = m;
                 __syncthreads();
                 m = 0;
-                for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i]);
-                __syncthreads();   // sred is rewritten for the next destination
+                for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i][k]);
                 amax = __uint_as_float(m);
                 s_tok = __fdiv_rn(TR::dmax, amax);
                 inv = __fdiv_rn(1.0f, s_tok);

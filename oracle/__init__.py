@@ -103,6 +103,10 @@ def _declare(lib):
     lib.oracle_dispatch_scaled.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, i32, i64, i64, vp, vp]
     lib.oracle_layout_masked.argtypes = [i32, i32, i32, i32, i32, vp, vp, i32, i64] + [vp] * 12
     lib.oracle_layout_masked.restype = i32
+    lib.oracle_token_layout.argtypes = [i32, i32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp]
+    lib.oracle_token_layout.restype = i64
+    lib.oracle_expert_token_rows.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp, vp, i32, vp]
+    lib.oracle_reduce_token_weights.argtypes = [i64, i32, vp, vp, vp]
     return lib
 
 
@@ -414,3 +418,83 @@ def combine_within_tolerance(got_bits: np.ndarray, ref: np.ndarray, mag: np.ndar
     sel = (np.abs(ref) >= np.ldexp(mag, -10)) & (ref != 0)
     rel = float(np.max(err[sel] / np.abs(ref[sel]))) if np.any(sel) else 0.0
     return bool(excess <= 0.0 and rel <= 1e-2), excess, rel
+
+
+# ---------------------------------------------------------------------------
+# per-rank receive layout (DeepEP recv_x / recv_topk_idx / recv_topk_weights)
+# ---------------------------------------------------------------------------
+
+class TokenLayout:
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def token_layout(R: int, T: int, E: int, K: int, topk: np.ndarray, w: np.ndarray,
+                 mask: np.ndarray | None = None) -> TokenLayout:
+    """One receive row per (token, destination rank); a masked entry (xActiveMask)
+    takes no part, like a -1 id."""
+    N = R * T
+    tk = np.ascontiguousarray(topk, dtype=np.int64).reshape(N, K).copy()
+    if mask is not None:
+        m = np.asarray(mask, np.uint8)
+        act = np.repeat(m.reshape(N, 1), K, 1) if m.size == N else m.reshape(N, K)
+        tk[act == 0] = -1
+    wf = np.ascontiguousarray(w, dtype=np.float32).reshape(N * K)
+    cap = max(N * min(R, K), 1)
+    tok_dst = np.zeros((N, K), np.int32)
+    src = np.zeros(cap, np.int32)
+    base = np.zeros(R + 1, np.int64)
+    ridx = np.zeros((cap, K), np.int64)
+    rw = np.zeros((cap, K), np.float32)
+    rows = load().oracle_token_layout(R, T, E, K, _p(tk), _p(wf), cap, _p(tok_dst), _p(src), _p(base),
+                                      _p(ridx), _p(rw))
+    return TokenLayout(R=R, T=T, E=E, K=K, L=E // R, rows=int(rows), tok_dst=tok_dst,
+                       recv_src=src[:rows], rank_tok_base=base, recv_topk_idx=ridx[:rows],
+                       recv_topk_weights=rw[:rows])
+
+
+def token_dispatch(tl: TokenLayout, x_bf16: np.ndarray, q: int):
+    """Receive rows of the per-rank layout (the same scatter, onto tok_dst)."""
+    N = tl.R * tl.T
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    H = x.shape[1]
+    db, sb = row_bytes(q, H)
+    data = np.zeros((tl.rows, db), np.uint8)
+    scales = np.zeros((tl.rows, sb), np.uint8)
+    dr = np.ascontiguousarray(tl.tok_dst.reshape(-1))
+    load().oracle_dispatch(N, tl.K, H, q, _p(dr), _p(x), 0, tl.rows, _p(data), _p(scales) if sb else None)
+    return data, scales
+
+
+def expert_token_rows(tl: TokenLayout, H: int, q: int, data: np.ndarray, scales: np.ndarray,
+                      mark_mod: int = 0) -> np.ndarray:
+    rows = np.arange(tl.rows, dtype=np.int64)
+    y = np.zeros((tl.rows, H), np.uint16)
+    d = np.ascontiguousarray(data, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    ridx = np.ascontiguousarray(tl.recv_topk_idx)
+    rw = np.ascontiguousarray(tl.recv_topk_weights)
+    load().oracle_expert_token_rows(tl.rows, _p(rows), H, tl.K, q, _p(d), _p(sc) if sc.size else None,
+                                    _p(ridx), _p(rw), mark_mod, _p(y))
+    return y
+
+
+def token_combine(tl: TokenLayout, y_bf16: np.ndarray, shared: np.ndarray | None = None):
+    """out = bf16(sum of the token's per-rank rows + shared rows), unit weights."""
+    ones = np.ones((tl.R, tl.T, tl.K), np.float32)
+    lay = Layout(R=tl.R, T=tl.T, K=tl.K, dst_row=tl.tok_dst)
+    return combine(lay, y_bf16, ones, shared)
+
+
+def token_combine_ref64(tl: TokenLayout, y_bf16: np.ndarray, shared: np.ndarray | None = None):
+    ones = np.ones((tl.R, tl.T, tl.K), np.float32)
+    lay = Layout(R=tl.R, T=tl.T, K=tl.K, dst_row=tl.tok_dst)
+    return combine_ref64(lay, y_bf16, ones, shared)
+
+
+def reduce_token_weights(tl: TokenLayout, rank_w: np.ndarray) -> np.ndarray:
+    N = tl.R * tl.T
+    out = np.zeros((N, tl.K), np.float32)
+    rw = np.ascontiguousarray(rank_w, dtype=np.float32)
+    load().oracle_reduce_token_weights(N, tl.K, _p(np.ascontiguousarray(tl.tok_dst)), _p(rw), _p(out))
+    return out

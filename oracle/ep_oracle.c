@@ -57,6 +57,10 @@ enum { S_NONE = 0, S_SCALAR = 1, S_CHANNEL = 2, S_EXPERT = 3 };
  * the page's per-group buffer rule aligns H to 128. */
 #define GROUP 128
 
+void oracle_expert_rows(int64_t nrows, const int64_t* rows, const int32_t* row_expert,
+                        int H, int q, const uint8_t* data, const uint8_t* scales,
+                        int mark_mod, uint16_t* y);
+
 /* Status values returned by oracle_layout. */
 enum { O_OK = 0, O_CAPACITY = 3, O_BAD_EXPERT = 4 };
 
@@ -465,6 +469,108 @@ int oracle_layout_masked(int R, int T, int E, int K, int alpha, const int64_t* t
                            expert_start, rank_base, src_prefix, dst_row, recv_src, expert_ids, usage);
     free(t2);
     return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Per-rank receive layout (DeepEP "Normal Mode API" dispatch returns:       */
+/* recv_x has one row per received token, recv_topk_idx / recv_topk_weights */
+/* give each received token's top-k as seen by the receiving rank).         */
+/*                                                                          */
+/* Rank j receives every source token (s,t) with is_token_in_rank[s,t,j]=1, */
+/* once, in (s, t) order; ranks are back to back.  For a received row,      */
+/* recv_topk_idx[k] is the local expert id e - j*L when topk[s,t,k] lives on */
+/* rank j and -1 otherwise; recv_topk_weights[k] is the token's weight for  */
+/* such a local expert and 0 otherwise.                                     */
+/*   tok_dst[R*T][K]   rows of the token on its destination ranks, in       */
+/*                     ascending rank order, -1 padded                      */
+/*   recv_src_tok[rows]  source token s*T+t of each row                     */
+/*   rank_tok_base[R+1]  first row of each rank; rank_tok_base[R] = rows    */
+/* Entries with ids outside [0, E) take no part.  Returns the row count.    */
+/* ------------------------------------------------------------------------ */
+int64_t oracle_token_layout(int R, int T, int E, int K, const int64_t* topk, const float* w,
+                            int64_t cap, int32_t* tok_dst, int32_t* recv_src_tok,
+                            int64_t* rank_tok_base, int64_t* recv_topk_idx,
+                            float* recv_topk_weights) {
+    int L = E / R;
+    int64_t N = (int64_t)R * T;
+    for (int64_t i = 0; i < N * K; ++i) tok_dst[i] = -1;
+    int32_t* nfill = (int32_t*)calloc((size_t)(N > 0 ? N : 1), sizeof(int32_t));
+    int64_t row = 0;
+    for (int j = 0; j < R; ++j) {
+        rank_tok_base[j] = row;
+        for (int64_t n = 0; n < N; ++n) {
+            int hit = 0;
+            for (int k = 0; k < K; ++k) {
+                int64_t e = topk[n * K + k];
+                if (e >= 0 && e < E && e / L == j) hit = 1;
+            }
+            if (!hit) continue;
+            tok_dst[n * K + nfill[n]] = (int32_t)row;
+            nfill[n] += 1;
+            if (row < cap) {
+                recv_src_tok[row] = (int32_t)n;
+                for (int k = 0; k < K; ++k) {
+                    int64_t e = topk[n * K + k];
+                    int local = (e >= 0 && e < E && e / L == j);
+                    recv_topk_idx[row * K + k] = local ? (e - (int64_t)j * L) : -1;
+                    recv_topk_weights[row * K + k] = local ? w[n * K + k] : 0.0f;
+                }
+            }
+            row += 1;
+        }
+    }
+    rank_tok_base[R] = row;
+    free(nfill);
+    return row;
+}
+
+/* Stand-in expert stage for per-rank rows: each rank applies its local
+ * experts to the received row and sums them with the received weights,
+ * y = bf16( sum_k recv_topk_weights[k] * 2^-(l_k mod mark_mod) * v ), k in
+ * order, each step acc = acc + (w * mark) * v, where v is the dequantised row
+ * (as oracle_expert_rows, no mark) and l_k the local expert id (mark_mod = 0:
+ * mark 1). */
+void oracle_expert_token_rows(int64_t nrows, const int64_t* rows, int H, int K, int q,
+                              const uint8_t* data, const uint8_t* scales,
+                              const int64_t* recv_topk_idx, const float* recv_topk_weights,
+                              int mark_mod, uint16_t* y) {
+    int32_t zero_expert = -1;
+    uint16_t* v = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+    int64_t db = oracle_row_data_bytes(q, H), sb = oracle_row_scale_bytes(q, H);
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t r = rows[i];
+        int64_t one = 0;
+        oracle_expert_rows(1, &one, &zero_expert, H, q, data + i * db, sb ? scales + i * sb : NULL, 0, v);
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int64_t l = recv_topk_idx[r * K + k];
+                if (l < 0) continue;
+                float mark = mark_mod > 0 ? ldexpf(1.0f, -(int)(l % mark_mod)) : 1.0f;
+                float coef = recv_topk_weights[r * K + k] * mark;
+                acc = acc + coef * oracle_bf16_to_f32(v[h]);
+            }
+            y[i * H + h] = oracle_bf16_from_f32(acc);
+        }
+    }
+    free(v);
+}
+
+/* Reduced weights of the per-rank combine (DeepEP combine returns the
+ * reduced topk weights): out_w[n][k] = sum over the token's rows i of
+ * rank_w[tok_dst[n][i]][k], rows in ascending rank order. */
+void oracle_reduce_token_weights(int64_t N, int K, const int32_t* tok_dst, const float* rank_w,
+                                 float* out_w) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) {
+            float acc = 0.0f;
+            for (int i = 0; i < K; ++i) {
+                int32_t r = tok_dst[n * K + i];
+                if (r < 0) continue;
+                acc = acc + rank_w[(int64_t)r * K + k];
+            }
+            out_w[n * K + k] = acc;
+        }
 }
 
 /* ------------------------------------------------------------------------ */

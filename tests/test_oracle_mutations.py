@@ -17,6 +17,7 @@ import test_oracle_dispatch_combine as tdc
 import test_oracle_layout as tl
 import test_oracle_quant as tq
 import test_oracle_quant_ext as tqx
+import test_oracle_token_layout as ttl
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ep_oracle.c")
 
@@ -54,6 +55,14 @@ MUTANTS = {
     "mask_token_index": ("int active = (mask_dims == 1) ? mask[i / K] : mask[i];",
                          "int active = (mask_dims == 1) ? mask[i % (R * T)] : mask[i];"),
     "smooth_scales_ignored": ("return smooth ? v * smooth[h] : v;", "return v;"),
+    "token_rank_of_expert_modulo": ("if (e >= 0 && e < E && e / L == j) hit = 1;",
+                                    "if (e >= 0 && e < E && e % R == j) hit = 1;"),
+    "token_global_expert_id": ("recv_topk_idx[row * K + k] = local ? (e - (int64_t)j * L) : -1;",
+                               "recv_topk_idx[row * K + k] = local ? e : -1;"),
+    "token_foreign_weights_kept": ("recv_topk_weights[row * K + k] = local ? w[n * K + k] : 0.0f;",
+                                   "recv_topk_weights[row * K + k] = w[n * K + k];"),
+    "token_reduce_skips_last_row": ("            for (int i = 0; i < K; ++i) {\n                int32_t r = tok_dst[n * K + i];",
+                                    "            for (int i = 0; i < K - 1; ++i) {\n                int32_t r = tok_dst[n * K + i];"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -82,6 +91,9 @@ def pins():
               lambda: tqx.test_dispatch_per_expert_scales_pick_the_entrys_expert(oracle.Q_INT8),
               lambda: tqx.test_masked_layout_matches_brute_force(0),
               lambda: tqx.test_masked_layout_matches_brute_force(1)]
+    cases += [lambda s=s: ttl.test_random_small_against_brute_force(s) for s in range(6)]
+    cases += [lambda: ttl.test_combine_through_rank_expert_stage_closed_form(2, 24, 4),
+              ttl.test_reduced_weights_equal_original_for_valid_entries]
     return cases
 
 
