@@ -38,12 +38,18 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s vs GB300 peak, 1 GPU"
-# key -> (workload index, quant mode, input-scale kind, xActiveMask dims)
-WORKLOAD_KEYS = {"1": (1, 0, 0, 0), "2": (2, 0, 0, 0), "3": (3, 2, 0, 0), "4a": (4, 4, 0, 0),
-                 "4b": (4, 6, 0, 0), "5": (5, 0, 0, 0),
+# key -> (workload index, quant mode, input-scale kind, xActiveMask dims, receive layout)
+# receive layout "expert": one row per (token, expert), grouped per expert (MAX);
+# "rank": one row per (token, destination rank) (DeepEP).
+WORKLOAD_KEYS = {"1": (1, 0, 0, 0, "expert"), "2": (2, 0, 0, 0, "expert"),
+                 "3": (3, 2, 0, 0, "expert"), "4a": (4, 4, 0, 0, "expert"),
+                 "4b": (4, 6, 0, 0, "expert"), "5": (5, 0, 0, 0, "expert"),
                  # further CANN quant modes and xActiveMask on the same shapes
-                 "4t": (4, 7, 0, 0), "4g": (4, 9, 0, 0), "3s": (3, 1, 2, 0), "3e": (3, 2, 3, 0),
-                 "5m": (5, 0, 0, 2)}
+                 "4t": (4, 7, 0, 0, "expert"), "4g": (4, 9, 0, 0, "expert"),
+                 "3s": (3, 1, 2, 0, "expert"), "3e": (3, 2, 3, 0, "expert"),
+                 "5m": (5, 0, 0, 2, "expert"),
+                 # the DeepEP per-rank receive layout
+                 "2r": (2, 0, 0, 0, "rank"), "4r": (4, 4, 0, 0, "rank")}
 QNAME = {0: "none", 1: "int8_static", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2",
          6: "mxfp4_e2m1", 7: "fp8_e4m3_per_token", 8: "fp8_e5m2_per_token",
          9: "fp8_e4m3_per_group128", 10: "fp8_e5m2_per_group128"}
@@ -202,17 +208,24 @@ def make_inputs(w, device):
     return topk, wts, x_dev, sh_dev
 
 
-def algorithmic_bytes(w, quant, rows, V):
+def algorithmic_bytes(w, quant, rows, V, per_rank=False):
+    """Bytes each kernel must move (reads + writes).  Expert layout: V gathered
+    rows in combine; per-rank layout: every receive row is gathered once (unit
+    weights, no weight reads)."""
     from combine_ep_layout_03_gb300 import ep
     db, sb = ep.ep_recv_row_bytes(w.H, quant)
     N, H, K, S = w.N, w.H, w.K, w.num_shared
     disp = N * H * 2 + N * K * 4 + rows * (db + sb)
-    comb = V * H * 2 + N * K * 8 + S * N * H * 2 + N * H * 2
     lay = N * K * 8 * 3 + N * K * 4 + rows * 4 + N * w.R
+    if per_rank:
+        comb = rows * H * 2 + N * K * 4 + S * N * H * 2 + N * H * 2
+        lay += N * K * (8 + 4 + 4) + rows * (4 + K * 12)
+    else:
+        comb = V * H * 2 + N * K * 8 + S * N * H * 2 + N * H * 2
     return {"layout": lay, "dispatch": disp, "combine": comb}
 
 
-def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0):
+def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_layout="expert"):
     from combine_ep_layout_03_gb300 import ep, synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -228,29 +241,54 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0):
         w_dev = torch.where(m3.reshape(w_dev.shape), w_dev, torch.zeros_like(w_dev))
     lay = ep.EPLayout(w.R, w.T, w.H, w.E, w.K, w.alpha, device=dev)
     lay.layout(topk_dev, active_mask=mask_dev)
-    rank_base = lay.recv_rows()
-    rows = int(rank_base[-1])
-    V = int((topk >= 0).sum())
+    per_rank = recv_layout == "rank"
+    if per_rank:
+        ridx, rw = lay.token_layout(topk_dev, w_dev, active_mask=mask_dev)
+        rows = int(lay.token_rows()[-1])
+    else:
+        rows = int(lay.recv_rows()[-1])
+    V = int((topk >= 0).sum()) if mask_dev is None else None
     data, scales = lay.alloc_recv(quant, max(rows, 1), device=dev)
+
+    def do_layout(topk_t, w_t, s=None):
+        lay.layout(topk_t, s, active_mask=mask_dev)
+        if per_rank:
+            lay.token_layout(topk_t, w_t, active_mask=mask_dev, stream=s, out=(ridx, rw))
+
+    def do_dispatch(x_t, s=None):
+        if per_rank:
+            lay.dispatch_tokens(x_t, quant, data, scales, s, scales=sc_dev, scale_kind=kind)
+        else:
+            lay.dispatch(x_t, quant, data, scales, s, scales=sc_dev, scale_kind=kind)
+
+    def do_combine(w_t, out_t, sh_t, s=None):
+        if per_rank:
+            lay.combine_tokens(y, out_t, sh_t, stream=s)
+        else:
+            lay.combine(y, w_t, out_t, sh_t, s)
+
     if quant == 0:
         y = data.view(torch.bfloat16).view(-1, w.H)
     else:
-        lay.dispatch(x_dev, quant, data, scales, scales=sc_dev, scale_kind=kind)
+        do_dispatch(x_dev)
         y = torch.empty((max(rows, 1), w.H), dtype=torch.bfloat16, device=dev)
-        lay.expert_identity(quant, data, scales, y)
+        lay.expert_identity(quant, data, scales, y) if not per_rank else \
+            lay.expert_identity_tokens(quant, data, scales, ridx, rw, y)
+    if V is None:
+        V = int(lay.views()["recv_cnt"].sum().item())
     out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        lay.layout(topk_dev, active_mask=mask_dev)
+        do_layout(topk_dev, w_dev)
         if ev is not None:
             ev[1].record(stream)
-        lay.dispatch(x_dev, quant, data, scales, scales=sc_dev, scale_kind=kind)
+        do_dispatch(x_dev)
         if ev is not None:
             ev[2].record(stream)
-        lay.combine(y, w_dev, out, sh_dev)
+        do_combine(w_dev, out, sh_dev)
         if ev is not None:
             ev[3].record(stream)
 
@@ -326,9 +364,9 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0):
                 s_k.wait_event(ev_in[i])
                 if i >= 2:
                     s_k.wait_event(ev_out[i - 2])         # slot's output already read back
-                lay.layout(sl["topk"], s_k, active_mask=mask_dev)
-                lay.dispatch(sl["x"], quant, data, scales, s_k, scales=sc_dev, scale_kind=kind)
-                lay.combine(y, sl["w"], sl["out"], sl["sh"], s_k)
+                do_layout(sl["topk"], sl["w"], s_k)
+                do_dispatch(sl["x"], s_k)
+                do_combine(sl["w"], sl["out"], sl["sh"], s_k)
                 ev_k[i].record(s_k)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_k[i])
@@ -356,7 +394,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0):
             assert torch.equal(out_host[(k2 - 1) % 2].to(dev), out)
 
     clocks = sampler.summary(t_timed0, t_timed1, t_warm0)
-    bytes_ = algorithmic_bytes(w, quant, rows, V)
+    bytes_ = algorithmic_bytes(w, quant, rows, V, per_rank)
     return dict(total_ms=total_ms, phase=phase, e2e=e2e, clocks=clocks, bytes=bytes_, rows=rows,
                 V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_dev, sh_dev=sh_dev)
 
@@ -421,6 +459,7 @@ def host_shared_lead(sh_dev, w, ranks=2):
 
 def workload_config(w, quant, key, kind=0, mask_dims=0):
     return {"workload": f"ep_layout_dispatch_combine[{key}] " + w.name,
+            "receive_layout": WORKLOAD_KEYS[key][4],
             "input_scales": SCALE_KIND[kind], "active_mask_dims": mask_dims,
             "R": w.R, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "alpha": w.alpha,
             "routing": w.routing, "drop_p": w.drop_p, "num_shared": w.num_shared,
@@ -434,7 +473,7 @@ def main(argv=None):
     args = parse_args(argv)
     rank, local_rank, world = dist_env()
     from combine_ep_layout_03_gb300 import synth
-    idx, quant, kind, mask_dims = WORKLOAD_KEYS[args.workload]
+    idx, quant, kind, mask_dims, recv_layout = WORKLOAD_KEYS[args.workload]
     w = synth.WORKLOADS[idx]
     if args.tokens_per_rank:
         w = w.with_(T=args.tokens_per_rank)
@@ -447,7 +486,7 @@ def main(argv=None):
     if world > 1:
         import datetime
         torch.distributed.init_process_group("gloo", timeout=datetime.timedelta(minutes=10))
-    res = run_ours(args, w, quant, rank, local_rank, world, kind, mask_dims)
+    res = run_ours(args, w, quant, rank, local_rank, world, kind, mask_dims, recv_layout)
     K = args.steps
     res["total_ms"], e2e_ms = max_over_ranks(
         [res["total_ms"], res["e2e"]["ms"] if res["e2e"] else 0.0], world)
@@ -494,7 +533,7 @@ def main(argv=None):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 5 * K,
+        "gpu_launches": (7 if recv_layout == "rank" else 5) * K,
         "clocks": res["clocks"],
         "kernels": {
             k: {"avg_ms": round(avg[k], 5), "median_ms": round(med[k], 5),

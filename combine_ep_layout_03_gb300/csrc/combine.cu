@@ -104,7 +104,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
         if (cnt > 0 && lane < a.K) {
             const int64_t n = blockIdx.x;
             dn = a.dst_row[n * a.K + lane];
-            wn = a.w[n * a.K + lane];
+            wn = a.w ? a.w[n * a.K + lane] : 1.0f;   // null weights: unit (per-rank rows)
         }
         bool ok = true;
         for (int64_t j = 0; j < cnt && ok; ++j) {
@@ -114,7 +114,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
             if (j + 1 < cnt && lane < a.K) {
                 const int64_t nn = n + G;
                 dn = a.dst_row[nn * a.K + lane];
-                wn = a.w[nn * a.K + lane];
+                wn = a.w ? a.w[nn * a.K + lane] : 1.0f;
             }
             const unsigned mask = __ballot_sync(0xffffffffu, d >= 0);
             const int kv = __popc(mask);
@@ -214,6 +214,34 @@ __device__ __forceinline__ float decode_mini(uint32_t c, int ebits, int mbits, i
     return sgn ? -mag : mag;
 }
 
+// Dequantised value of element h of a receive row (before any bf16 rounding).
+template <int Q>
+__device__ __forceinline__ float dequant_one(const uint8_t* row, const uint8_t* srow, int h) {
+    if (Q == M_NONE) {
+        return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[h]);
+    } else if (Q == M_INT8) {
+        const float inv = reinterpret_cast<const float*>(srow)[0];
+        return __fmul_rn((float)(int8_t)row[h], inv);
+    } else if (Q == M_INT8S) {
+        return (float)(int8_t)row[h];
+    } else if (Q == M_FP8T_E4M3 || Q == M_FP8T_E5M2 || Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2) {
+        const bool grp = (Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2);
+        const float inv = reinterpret_cast<const float*>(srow)[grp ? (h >> 7) : 0];
+        const float cv = (Q == M_FP8T_E4M3 || Q == M_FP8G_E4M3) ? decode_mini(row[h], 4, 3, 7)
+                                                                 : decode_mini(row[h], 5, 2, 15);
+        return __fmul_rn(cv, inv);
+    } else {
+        uint32_t c;
+        if (Q == M_E2M1) c = (row[h >> 1] >> (4 * (h & 1))) & 0xfu;
+        else c = row[h];
+        float cv;
+        if (Q == M_E4M3) cv = decode_mini(c, 4, 3, 7);
+        else if (Q == M_E5M2) cv = decode_mini(c, 5, 2, 15);
+        else cv = decode_mini(c, 2, 1, 1);
+        return __fmul_rn(cv, pow2i((int)srow[h >> 5] - 127));
+    }
+}
+
 template <int Q>
 __global__ void __launch_bounds__(256)
 identity_kernel(IdentityArgs a) {
@@ -234,34 +262,72 @@ identity_kernel(IdentityArgs a) {
         const uint8_t* srow = a.scales ? a.scales + r * a.scale_bytes : nullptr;
         uint16_t* yrow = a.y + r * a.H;
         for (int h2 = threadIdx.x; h2 < a.H / 2; h2 += blockDim.x) {
+            const float f0 = __fmul_rn(dequant_one<Q>(row, srow, 2 * h2), mark);
+            const float f1 = __fmul_rn(dequant_one<Q>(row, srow, 2 * h2 + 1), mark);
+            reinterpret_cast<uint32_t*>(yrow)[h2] = pack_bf16x2_rn(f0, f1);
+        }
+    }
+}
+
+// Reduced weights of the per-rank combine (DeepEP combine returns the
+// reduced topk weights): out_w[n][k] = sum over the token's rows i, in
+// ascending rank order, of rank_w[tok_dst[n][i]][k].
+__global__ void reduce_token_weights_kernel(const int32_t* tok_dst, const float* rank_w, float* out_w,
+                                            int64_t N, int K, const int32_t* tok_meta, int64_t cap) {
+    if ((int64_t)tok_meta[1] > cap) return;   // rows beyond rank_w: combine reports the capacity error
+    const int64_t total = N * K;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = g / K;
+        const int k = (int)(g - n * K);
+        float acc = 0.0f;
+        for (int i = 0; i < K; ++i) {
+            const int r = tok_dst[n * K + i];
+            if (r >= 0) acc = __fadd_rn(acc, rank_w[(int64_t)r * K + k]);
+        }
+        out_w[g] = acc;
+    }
+}
+
+// Stand-in expert stage of the per-rank layout: each received row goes through
+// the rank's local experts (identity, times 2^-(l mod mark_mod) for local
+// expert l) weighted by the received weights, summed in slot order:
+// y = bf16( sum_k (w_k * mark_k) * v ), v the dequantised row rounded to bf16.
+template <int Q>
+__global__ void __launch_bounds__(256)
+identity_tokens_kernel(IdentityArgs a, const int64_t* ridx, const float* rw, int K) {
+    const int total = a.expert_base[a.E];
+    if ((int64_t)total > a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
+        return;
+    }
+    __shared__ float coef[kMaxTopk];
+    for (int64_t r = blockIdx.x; r < total; r += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < K) {
+            const int64_t l = ridx[r * K + threadIdx.x];
+            float c = 0.0f;
+            if (l >= 0) {
+                const float mark = a.mark_mod > 0 ? pow2i(-(int)(l % a.mark_mod)) : 1.0f;
+                c = __fmul_rn(rw[r * K + threadIdx.x], mark);
+            }
+            coef[threadIdx.x] = l >= 0 ? c : __int_as_float(0x7fc00000);   // NaN marks "not local"
+        }
+        __syncthreads();
+        const uint8_t* row = a.data + r * a.row_bytes;
+        const uint8_t* srow = a.scales ? a.scales + r * a.scale_bytes : nullptr;
+        uint16_t* yrow = a.y + r * a.H;
+        for (int h2 = threadIdx.x; h2 < a.H / 2; h2 += blockDim.x) {
             float f[2];
             for (int i = 0; i < 2; ++i) {
-                const int h = 2 * h2 + i;
-                float v;
-                if (Q == M_NONE) {
-                    v = bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[h]);
-                } else if (Q == M_INT8) {
-                    const float inv = reinterpret_cast<const float*>(srow)[0];
-                    v = __fmul_rn((float)(int8_t)row[h], inv);
-                } else if (Q == M_INT8S) {
-                    v = (float)(int8_t)row[h];
-                } else if (Q == M_FP8T_E4M3 || Q == M_FP8T_E5M2 || Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2) {
-                    const bool grp = (Q == M_FP8G_E4M3 || Q == M_FP8G_E5M2);
-                    const float inv = reinterpret_cast<const float*>(srow)[grp ? (h >> 7) : 0];
-                    const float cv = (Q == M_FP8T_E4M3 || Q == M_FP8G_E4M3) ? decode_mini(row[h], 4, 3, 7)
-                                                                             : decode_mini(row[h], 5, 2, 15);
-                    v = __fmul_rn(cv, inv);
-                } else {
-                    uint32_t c;
-                    if (Q == M_E2M1) c = (row[h >> 1] >> (4 * (h & 1))) & 0xfu;
-                    else c = row[h];
-                    float cv;
-                    if (Q == M_E4M3) cv = decode_mini(c, 4, 3, 7);
-                    else if (Q == M_E5M2) cv = decode_mini(c, 5, 2, 15);
-                    else cv = decode_mini(c, 2, 1, 1);
-                    v = __fmul_rn(cv, pow2i((int)srow[h >> 5] - 127));
+                const float vb = bf16_bits_to_float(
+                    (uint32_t)(pack_bf16x2_rn(dequant_one<Q>(row, srow, 2 * h2 + i), 0.0f) & 0xffffu));
+                float acc = 0.0f;
+                for (int k = 0; k < K; ++k) {
+                    const float ck = coef[k];
+                    if (ck == ck) acc = __fadd_rn(acc, __fmul_rn(ck, vb));
                 }
-                f[i] = __fmul_rn(v, mark);
+                f[i] = acc;
             }
             reinterpret_cast<uint32_t*>(yrow)[h2] = pack_bf16x2_rn(f[0], f[1]);
         }
@@ -323,6 +389,34 @@ cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant
         case M_FP8T_E5M2: identity_kernel<M_FP8T_E5M2><<<grid, 256, 0, st>>>(a); break;
         case M_FP8G_E4M3: identity_kernel<M_FP8G_E4M3><<<grid, 256, 0, st>>>(a); break;
         case M_FP8G_E5M2: identity_kernel<M_FP8G_E5M2><<<grid, 256, 0, st>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_token_weights(const ep_handle* h, const float* rank_w, float* out_w,
+                                        int64_t cap, cudaStream_t st) {
+    if (h->N == 0) return cudaSuccess;
+    reduce_token_weights_kernel<<<h->num_sms * 4, 256, 0, st>>>(h->tok_dst, rank_w, out_w, h->N, h->K,
+                                                                h->tok_meta, cap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_identity_tokens(const ep_handle* h, const IdentityArgs& a, const int64_t* ridx,
+                                   const float* rw, int quant, cudaStream_t st) {
+    const int grid = h->num_sms * 8;
+    const int K = h->K;
+    switch (quant) {
+        case M_NONE: identity_tokens_kernel<M_NONE><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_INT8S: identity_tokens_kernel<M_INT8S><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_INT8: identity_tokens_kernel<M_INT8><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_E4M3: identity_tokens_kernel<M_E4M3><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_E5M2: identity_tokens_kernel<M_E5M2><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_E2M1: identity_tokens_kernel<M_E2M1><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_FP8T_E4M3: identity_tokens_kernel<M_FP8T_E4M3><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_FP8T_E5M2: identity_tokens_kernel<M_FP8T_E5M2><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_FP8G_E4M3: identity_tokens_kernel<M_FP8G_E4M3><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
+        case M_FP8G_E5M2: identity_tokens_kernel<M_FP8G_E5M2><<<grid, 256, 0, st>>>(a, ridx, rw, K); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -50,10 +50,17 @@ int64_t recv_cap_of(const ep_params* p) {
     return p->recv_capacity_rows > 0 ? p->recv_capacity_rows : worst_rows(p);
 }
 
+// Rows of the per-rank layout: a token reaches at most min(R, K) ranks.
+int64_t tok_cap_of(const ep_params* p) {
+    const int64_t m = p->num_ranks < p->topk ? p->num_ranks : p->topk;
+    return (int64_t)p->num_ranks * p->tokens_per_rank * m;
+}
+
 // Byte offsets of every workspace array, in one place.
 struct Carve {
     size_t status, blk_hist, blk_rank, cnt, itr, ntpr, recv_cnt, aligned, expert_start,
-        rank_base, expert_base, src_prefix, dst_row, recv_src, expert_ids, usage, total;
+        rank_base, expert_base, src_prefix, dst_row, recv_src, expert_ids, usage,
+        tok_dst, recv_src_tok, tok_blk, tok_total, tok_base, tok_meta, total;
 };
 
 Carve carve_of(const ep_params* p) {
@@ -79,6 +86,12 @@ Carve carve_of(const ep_params* p) {
     c.recv_src = take(sizeof(int32_t) * (size_t)recv_cap_of(p));
     c.expert_ids = take(sizeof(int32_t) * (size_t)(R * L));
     c.usage = take(sizeof(int32_t) * (size_t)(R * 2));
+    c.tok_dst = take(sizeof(int32_t) * (size_t)(N * K));
+    c.recv_src_tok = take(sizeof(int32_t) * (size_t)tok_cap_of(p));
+    c.tok_blk = take(sizeof(int32_t) * (size_t)t.B * R);
+    c.tok_total = take(sizeof(int32_t) * (size_t)R);
+    c.tok_base = take(sizeof(int64_t) * (size_t)(R + 1));
+    c.tok_meta = take(sizeof(int32_t) * 4);
     c.total = off;
     return c;
 }
@@ -191,6 +204,13 @@ ep_status ep_handle_create(const ep_params* p, void* workspace, size_t workspace
     h->recv_src = (int32_t*)(w + c.recv_src);
     h->expert_ids = (int32_t*)(w + c.expert_ids);
     h->usage = (int32_t*)(w + c.usage);
+    h->tok_cap = tok_cap_of(p);
+    h->tok_dst = (int32_t*)(w + c.tok_dst);
+    h->recv_src_tok = (int32_t*)(w + c.recv_src_tok);
+    h->tok_blk = (int32_t*)(w + c.tok_blk);
+    h->tok_total = (int32_t*)(w + c.tok_total);
+    h->tok_base = (int64_t*)(w + c.tok_base);
+    h->tok_meta = (int32_t*)(w + c.tok_meta);
     *out = h;
     return EP_OK;
 }
@@ -229,6 +249,10 @@ ep_status ep_handle_views(const ep_handle* h, ep_layout_views* v) {
     v->expert_ids = h->expert_ids;
     v->expert_usage_stats = h->usage;
     v->recv_src_capacity = h->recv_cap;
+    v->tok_dst = h->tok_dst;
+    v->recv_src_tok = h->recv_src_tok;
+    v->rank_tok_base = h->tok_base;
+    v->tok_capacity = h->tok_cap;
     return EP_OK;
 }
 
@@ -262,9 +286,13 @@ ep_status ep_dispatch(const ep_handle* hc, const void* x, ep_quant_mode q, void*
     return ep_dispatch_scaled(hc, x, q, nullptr, EP_SCALES_NONE, recv_data, recv_scales, cap, stream);
 }
 
-ep_status ep_dispatch_scaled(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
-                             ep_scale_kind kind, void* recv_data, void* recv_scales, int64_t cap,
-                             ep_stream_t stream) {
+namespace {
+
+// Shared body of ep_dispatch_scaled and ep_dispatch_tokens: tokens == true
+// targets the per-rank layout (tok_dst, one segment without padding).
+ep_status dispatch_impl(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
+                        ep_scale_kind kind, void* recv_data, void* recv_scales, int64_t cap,
+                        ep_stream_t stream, bool tokens) {
     ep_handle* h = const_cast<ep_handle*>(hc);
     if (!h) return EP_ERR_INVALID_ARG;
     if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
@@ -290,16 +318,125 @@ ep_status ep_dispatch_scaled(const ep_handle* hc, const void* x, ep_quant_mode q
     a.smooth_kind = (int32_t)kind;
     a.data = (uint8_t*)recv_data;
     a.scales = (uint8_t*)recv_scales;
-    a.dst_row = h->dst_row;
-    a.expert_base = h->expert_base;
-    a.recv_cnt = h->recv_cnt;
+    a.dst_row = tokens ? h->tok_dst : h->dst_row;
+    a.expert_base = tokens ? h->tok_meta : h->expert_base;      // {0, rows}: one segment
+    a.recv_cnt = tokens ? h->tok_meta + 2 : h->recv_cnt;        // {rows}: no padding
     a.status = h->status;
     a.N = h->N;
     a.cap = cap;
-    a.H = h->H; a.K = h->K; a.E = h->E; a.nvec = h->H / 8;
+    a.H = h->H; a.K = h->K; a.E = tokens ? 1 : h->E; a.nvec = h->H / 8;
     a.row_bytes = (int32_t)db;
     a.scale_bytes = (int32_t)sb;
     return from_cuda(launch_dispatch(h, a, (int)q, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+ep_status ep_dispatch_scaled(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
+                             ep_scale_kind kind, void* recv_data, void* recv_scales, int64_t cap,
+                             ep_stream_t stream) {
+    return dispatch_impl(hc, x, q, scales, kind, recv_data, recv_scales, cap, stream, false);
+}
+
+ep_status ep_dispatch_tokens(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
+                             ep_scale_kind kind, void* recv_data, void* recv_scales, int64_t cap,
+                             ep_stream_t stream) {
+    if (kind == EP_SCALES_PER_EXPERT) return EP_ERR_UNSUPPORTED;
+    return dispatch_impl(hc, x, q, scales, kind, recv_data, recv_scales, cap, stream, true);
+}
+
+ep_status ep_token_layout(ep_handle* h, const int64_t* topk, const float* w, const uint8_t* mask,
+                          int32_t mask_dims, int64_t* recv_topk_idx, float* recv_topk_weights,
+                          int64_t rows_cap, ep_stream_t stream) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (rows_cap < 0) return EP_ERR_INVALID_ARG;
+    if (h->N > 0 && (!topk || !aligned_to(topk, 8) || !w || !aligned_to(w, 4))) return EP_ERR_INVALID_ARG;
+    if (rows_cap > 0 && (!recv_topk_idx || !recv_topk_weights)) return EP_ERR_INVALID_ARG;
+    if (mask && mask_dims != 1 && mask_dims != 2) return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    TokenLayoutArgs a;
+    a.topk = topk; a.w = w; a.mask = mask; a.mask_dims = mask ? mask_dims : 0;
+    a.R = h->R; a.T = h->T; a.E = h->E; a.K = h->K; a.L = h->L; a.C = h->C; a.TPB = h->TPB; a.B = h->B;
+    a.tok_cap = h->tok_cap;
+    a.rows_cap = rows_cap;
+    a.status = h->status;
+    a.blk_rank = h->blk_rank;
+    a.tok_blk = h->tok_blk;
+    a.tok_total = h->tok_total;
+    a.tok_base = h->tok_base;
+    a.tok_meta = h->tok_meta;
+    a.tok_dst = h->tok_dst;
+    a.recv_src_tok = h->recv_src_tok;
+    a.recv_topk_idx = recv_topk_idx;
+    a.recv_topk_weights = recv_topk_weights;
+    return from_cuda(launch_token_layout(h, a, (cudaStream_t)stream));
+}
+
+ep_status ep_handle_token_rows(const ep_handle* h, int64_t* host, ep_stream_t stream) {
+    if (!h || !host) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
+    return from_cuda(cudaMemcpy(host, h->tok_base, sizeof(int64_t) * (size_t)(h->R + 1),
+                                cudaMemcpyDeviceToHost));
+}
+
+ep_status ep_combine_tokens(const ep_handle* hc, const void* y, int64_t y_cap, const void* shared,
+                            int32_t S, void* out, const float* rank_w, float* out_w,
+                            ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (S < 0 || S > kMaxShared || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
+    if (y_cap < 0) return EP_ERR_INVALID_ARG;
+    if ((rank_w == nullptr) != (out_w == nullptr)) return EP_ERR_INVALID_ARG;
+    if (h->N > 0) {
+        if (!out || !aligned_to(out, 16)) return EP_ERR_INVALID_ARG;
+        if (y_cap > 0 && (!y || !aligned_to(y, 16))) return EP_ERR_INVALID_ARG;
+    }
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    CombineArgs a;
+    a.y = (const uint16_t*)y;
+    a.w = nullptr;                    // unit weights: rows are already weighted per rank
+    a.shared = (const uint16_t*)shared;
+    a.out = (uint16_t*)out;
+    a.dst_row = h->tok_dst;
+    a.expert_base = h->tok_meta;
+    a.status = h->status;
+    a.N = h->N;
+    a.cap = y_cap;
+    a.T = h->T; a.H = h->H; a.K = h->K; a.E = 1; a.S = S; a.nvec = h->H / 8;
+    cudaError_t err = launch_combine(h, a, (cudaStream_t)stream);
+    if (err == cudaSuccess && rank_w)
+        err = launch_reduce_token_weights(h, rank_w, out_w, y_cap, (cudaStream_t)stream);
+    return from_cuda(err);
+}
+
+ep_status ep_expert_identity_tokens(const ep_handle* hc, ep_quant_mode q, const void* recv_data,
+                                    const void* recv_scales, const int64_t* ridx, const float* rw,
+                                    int64_t cap, int32_t mark_mod, void* y, ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    if (is_mx(q) && h->H % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (is_group(q) && h->H % 128 != 0) return EP_ERR_INVALID_ARG;
+    if (cap < 0 || mark_mod < 0) return EP_ERR_INVALID_ARG;
+    if (cap > 0 && (!recv_data || !y || !aligned_to(y, 4) || !ridx || !rw)) return EP_ERR_INVALID_ARG;
+    if (q != EP_QUANT_NONE && q != EP_QUANT_INT8_STATIC && cap > 0 && !recv_scales) return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    int64_t db = 0, sb = 0;
+    ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);
+    if (s != EP_OK) return s;
+    IdentityArgs a;
+    a.data = (const uint8_t*)recv_data;
+    a.scales = (const uint8_t*)recv_scales;
+    a.y = (uint16_t*)y;
+    a.expert_base = h->tok_meta;
+    a.recv_src = h->recv_src_tok;
+    a.status = h->status;
+    a.cap = cap;
+    a.recv_src_cap = h->tok_cap;
+    a.H = h->H; a.E = 1; a.nvec = h->H / 8;
+    a.row_bytes = (int32_t)db; a.scale_bytes = (int32_t)sb; a.mark_mod = mark_mod;
+    return from_cuda(launch_identity_tokens(h, a, ridx, rw, (int)q, (cudaStream_t)stream));
 }
 
 ep_status ep_combine(const ep_handle* hc, const void* y, int64_t y_cap, const float* w,

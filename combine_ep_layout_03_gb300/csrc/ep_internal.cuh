@@ -49,6 +49,14 @@ struct ep_handle {
     int32_t* recv_src;      // [recv_cap]
     int32_t* expert_ids;    // [R][L]
     int32_t* usage;         // [R][2]
+    // per-rank receive layout (one row per token and destination rank)
+    int64_t tok_cap;        // rows of recv_src_tok = N * min(R, K)
+    int32_t* tok_dst;       // [N][K] rows of the token on its ranks (ascending), -1 padded
+    int32_t* recv_src_tok;  // [tok_cap]
+    int32_t* tok_blk;       // [B][R] per-CTA exclusive prefix of tokens per destination rank
+    int32_t* tok_total;     // [R] tokens received by each rank
+    int64_t* tok_base;      // [R+1] first row of each rank
+    int32_t* tok_meta;      // [4] {0, rows, rows, 0}: one segment, no padding
 };
 
 // Argument block shared by the three layout kernels.
@@ -74,6 +82,27 @@ struct LayoutArgs {
     int32_t* recv_src;
     int32_t* expert_ids;
     int32_t* usage;
+};
+
+// Arguments of the per-rank (token) layout kernels.
+struct TokenLayoutArgs {
+    const int64_t* topk;
+    const float* w;           // topk_weights [N][K]
+    const uint8_t* mask;
+    int32_t mask_dims;
+    int32_t R, T, E, K, L, C, TPB, B;
+    int64_t tok_cap;          // recv_src_tok rows
+    int64_t rows_cap;         // recv_topk_idx / recv_topk_weights rows
+    int32_t* status;
+    const int32_t* blk_rank;  // [B][R] tokens per destination rank per CTA (count kernel)
+    int32_t* tok_blk;
+    int32_t* tok_total;
+    int64_t* tok_base;
+    int32_t* tok_meta;
+    int32_t* tok_dst;
+    int32_t* recv_src_tok;
+    int64_t* recv_topk_idx;   // [rows_cap][K]
+    float* recv_topk_weights; // [rows_cap][K]
 };
 
 struct DispatchArgs {
@@ -123,6 +152,11 @@ cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t
 cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st);
 cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant, cudaStream_t st);
+cudaError_t launch_token_layout(const ep_handle* h, const TokenLayoutArgs& a, cudaStream_t st);
+cudaError_t launch_reduce_token_weights(const ep_handle* h, const float* rank_w, float* out_w,
+                                        int64_t cap, cudaStream_t st);
+cudaError_t launch_identity_tokens(const ep_handle* h, const IdentityArgs& a, const int64_t* ridx,
+                                   const float* rw, int quant, cudaStream_t st);
 
 // Device helpers shared by the kernels of this library.
 __device__ __forceinline__ void ep_set_status(int32_t* status, int code) {

@@ -260,6 +260,140 @@ layout_assign_kernel(LayoutArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- per-rank layout
+// DeepEP receive layout: one row per (token, destination rank), rank by rank,
+// tokens in (source rank, token) order.  Built from the count kernel's per-CTA
+// tokens-per-rank counts: a column scan per rank, then a warp-ordered walk in
+// which the token's distinct destination ranks are found with __match_any_sync
+// and ranked in ascending order; per-(warp, rank) running counters fix rows.
+
+__device__ __forceinline__ int64_t token_entry_expert(const TokenLayoutArgs& a, int64_t i) {
+    const int64_t e = a.topk[i];
+    if (a.mask) {
+        const uint8_t act = a.mask_dims == 1 ? a.mask[i / a.K] : a.mask[i];
+        if (!act) return -1;
+    }
+    return (e >= 0 && e < a.E) ? e : -1;
+}
+
+// CTA j: exclusive prefix over CTAs of the tokens each CTA sends to rank j.
+__global__ void __launch_bounds__(kLayoutThreads)
+token_scan_kernel(TokenLayoutArgs a) {
+    extern __shared__ int sm[];
+    const int j = blockIdx.x, B = a.B;
+    int* vals = sm;              // [B]
+    int* pre = sm + B;           // [B+1]
+    int* scratch = pre + B + 1;  // [NW+1]
+    for (int b = threadIdx.x; b < B; b += blockDim.x) vals[b] = a.blk_rank[(int64_t)b * a.R + j];
+    __syncthreads();
+    block_exclusive_scan(vals, pre, B, scratch);
+    for (int b = threadIdx.x; b < B; b += blockDim.x) a.tok_blk[(int64_t)b * a.R + j] = pre[b];
+    if (threadIdx.x == 0) a.tok_total[j] = pre[B];
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+token_assign_kernel(TokenLayoutArgs a) {
+    extern __shared__ int sm[];
+    constexpr int NW = kLayoutThreads / 32;
+    const int R = a.R, K = a.K;
+    int* tot = sm;                  // [R]
+    int* base = tot + R;            // [R+1] first row of each rank
+    int* scratch = base + R + 1;    // [NW+1]
+    int* wc = scratch + NW + 1;     // [NW][R] per-warp running rows
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int j = tid; j < R; j += blockDim.x) tot[j] = a.tok_total[j];
+    __syncthreads();
+    block_exclusive_scan(tot, base, R, scratch);
+    const int b = blockIdx.x;
+    const int64_t total = base[R];
+    if (b == 0) {
+        for (int j = tid; j <= R; j += blockDim.x) a.tok_base[j] = base[j];
+        if (tid == 0) {
+            a.tok_meta[0] = 0;
+            a.tok_meta[1] = (int32_t)total;
+            a.tok_meta[2] = (int32_t)total;
+            a.tok_meta[3] = 0;
+            if (total > a.tok_cap || total > a.rows_cap) ep_set_status(a.status, EP_ERR_CAPACITY);
+        }
+    }
+    const int s = b / a.C, c = b - (b / a.C) * a.C;
+    const int t0 = c * a.TPB;
+    const int t1 = min(a.T, t0 + a.TPB);
+    if (t1 <= t0) return;
+    const int ntok = t1 - t0;
+    const int per = (ntok + NW - 1) / NW;
+    const int w0 = min(ntok, warp * per), w1 = min(ntok, w0 + per);
+    int* mycnt = wc + warp * R;
+    for (int j = lane; j < R; j += 32) mycnt[j] = 0;
+    __syncwarp();
+    const int64_t n0 = (int64_t)s * a.T + t0;
+    // phase A: tokens per destination rank in this warp's range
+    for (int tt = w0; tt < w1; ++tt) {
+        const int64_t n = n0 + tt;
+        int rk = -1;
+        if (lane < K) {
+            const int64_t e = token_entry_expert(a, n * K + lane);
+            if (e >= 0) rk = (int)(e / a.L);
+        }
+        const unsigned peers = __match_any_sync(kFull, rk);
+        if (rk >= 0 && lane == __ffs(peers) - 1) mycnt[rk] += 1;   // distinct ranks: no clash
+        __syncwarp();
+    }
+    __syncthreads();
+    // phase B: first row of each (warp, rank) = rank base + CTA prefix + earlier warps
+    for (int j = tid; j < R; j += blockDim.x) {
+        int run = base[j] + a.tok_blk[(int64_t)b * R + j];
+        for (int w = 0; w < NW; ++w) {
+            const int v = wc[w * R + j];
+            wc[w * R + j] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    // phase C: ordered walk; a token's ranks are ordered ascending
+    for (int tt = w0; tt < w1; ++tt) {
+        const int64_t n = n0 + tt;
+        int64_t e = -1;
+        int rk = -1;
+        float wt = 0.0f;
+        if (lane < K) {
+            e = token_entry_expert(a, n * K + lane);
+            if (e >= 0) rk = (int)(e / a.L);
+            wt = a.w[n * K + lane];
+        }
+        const unsigned peers = __match_any_sync(kFull, rk);
+        const bool first = rk >= 0 && lane == __ffs(peers) - 1;
+        const unsigned firsts = __ballot_sync(kFull, first);
+        const int ndist = __popc(firsts);
+        int ord = 0;
+        for (int k2 = 0; k2 < K; ++k2) {
+            const int r2 = __shfl_sync(kFull, rk, k2);
+            if (((firsts >> k2) & 1u) && r2 < rk) ++ord;
+        }
+        int row = -1;
+        if (first) row = mycnt[rk];
+        __syncwarp();
+        if (first) mycnt[rk] = row + 1;
+        __syncwarp();
+        if (first) {
+            a.tok_dst[n * K + ord] = row;
+            if (row < a.tok_cap) a.recv_src_tok[row] = (int32_t)n;
+        }
+        if (lane < K && lane >= ndist) a.tok_dst[n * K + lane] = -1;
+        for (int i = 0; i < ndist; ++i) {
+            const unsigned m = __ballot_sync(kFull, first && ord == i);
+            const int src = __ffs(m) - 1;
+            const int ri = __shfl_sync(kFull, row, src);
+            const int ji = __shfl_sync(kFull, rk, src);
+            if (lane < K && ri < a.rows_cap) {
+                const bool loc = (rk == ji);
+                a.recv_topk_idx[(int64_t)ri * K + lane] = loc ? e - (int64_t)ji * a.L : -1;
+                a.recv_topk_weights[(int64_t)ri * K + lane] = loc ? wt : 0.0f;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t* mask,
@@ -292,5 +426,16 @@ cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t
     constexpr int NW = kLayoutThreads / 32;
     const size_t smem_assign = sizeof(int) * (size_t)(3 * h->E + 1 + NW + 1 + NW * h->E);
     layout_assign_kernel<<<h->B, kLayoutThreads, smem_assign, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_token_layout(const ep_handle* h, const TokenLayoutArgs& a, cudaStream_t st) {
+    constexpr int NW = kLayoutThreads / 32;
+    const size_t smem_scan = sizeof(int) * (size_t)(2 * h->B + 1 + NW + 1);
+    token_scan_kernel<<<h->R, kLayoutThreads, smem_scan, st>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const size_t smem_assign = sizeof(int) * (size_t)(2 * h->R + 1 + NW + 1 + NW * h->R);
+    token_assign_kernel<<<h->B, kLayoutThreads, smem_assign, st>>>(a);
     return cudaGetLastError();
 }

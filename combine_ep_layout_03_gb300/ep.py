@@ -53,7 +53,9 @@ class ep_layout_views(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt", "aligned_cnt",
         "expert_start", "rank_base", "expert_base", "src_prefix", "dst_row", "recv_src",
-        "expert_ids", "expert_usage_stats")] + [("recv_src_capacity", ctypes.c_int64)]
+        "expert_ids", "expert_usage_stats")] + [("recv_src_capacity", ctypes.c_int64)] + [
+        ("tok_dst", ctypes.c_void_p), ("recv_src_tok", ctypes.c_void_p),
+        ("rank_tok_base", ctypes.c_void_p), ("tok_capacity", ctypes.c_int64)]
 
 
 class ep_layout_outputs(ctypes.Structure):
@@ -88,6 +90,11 @@ def _load():
         "ep_combine": ([vp, vp, i64, vp, vp, i32, vp, vp], st),
         "ep_expert_identity": ([vp, st, vp, vp, i64, i32, vp, vp], st),
         "ep_layout_static_scratch": ([P, vp, ctypes.POINTER(ep_layout_outputs), vp], st),
+        "ep_token_layout": ([vp, vp, vp, vp, i32, vp, vp, i64, vp], st),
+        "ep_handle_token_rows": ([vp, vp, vp], st),
+        "ep_dispatch_tokens": ([vp, vp, st, vp, st, vp, vp, i64, vp], st),
+        "ep_combine_tokens": ([vp, vp, i64, vp, i32, vp, vp, vp, vp], st),
+        "ep_expert_identity_tokens": ([vp, st, vp, vp, vp, vp, i64, i32, vp, vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -216,6 +223,42 @@ def ep_expert_identity(h: int, quant: int, recv_data, recv_scales, rows_capacity
            "ep_expert_identity")
 
 
+def ep_token_layout(h: int, topk_idx, topk_weights, mask, mask_dims: int, recv_topk_idx,
+                    recv_topk_weights, rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_token_layout(h, _ptr(topk_idx), _ptr(topk_weights), _ptr(mask), int(mask_dims),
+                                _ptr(recv_topk_idx), _ptr(recv_topk_weights), int(rows_capacity),
+                                _stream(stream)), "ep_token_layout")
+
+
+def ep_handle_token_rows(h: int, R: int, stream=None) -> list[int]:
+    buf = (ctypes.c_int64 * (R + 1))()
+    _check(_lib.ep_handle_token_rows(h, ctypes.addressof(buf), _stream(stream)), "ep_handle_token_rows")
+    return list(buf)
+
+
+def ep_dispatch_tokens(h: int, x, quant: int, scales, scale_kind: int, recv_data, recv_scales,
+                       recv_rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_dispatch_tokens(h, _ptr(x), quant, _ptr(scales), int(scale_kind), _ptr(recv_data),
+                                   _ptr(recv_scales), int(recv_rows_capacity), _stream(stream)),
+           "ep_dispatch_tokens")
+
+
+def ep_combine_tokens(h: int, y, y_rows_capacity: int, shared, num_shared: int, out, rank_weights,
+                      out_weights, stream=None) -> None:
+    _check(_lib.ep_combine_tokens(h, _ptr(y), int(y_rows_capacity), _ptr(shared), int(num_shared),
+                                  _ptr(out), _ptr(rank_weights), _ptr(out_weights), _stream(stream)),
+           "ep_combine_tokens")
+
+
+def ep_expert_identity_tokens(h: int, quant: int, recv_data, recv_scales, recv_topk_idx,
+                              recv_topk_weights, rows_capacity: int, mark_mod: int, y,
+                              stream=None) -> None:
+    _check(_lib.ep_expert_identity_tokens(h, quant, _ptr(recv_data), _ptr(recv_scales),
+                                          _ptr(recv_topk_idx), _ptr(recv_topk_weights),
+                                          int(rows_capacity), int(mark_mod), _ptr(y), _stream(stream)),
+           "ep_expert_identity_tokens")
+
+
 # ---------------------------------------------------------------- convenience wrapper
 
 _VIEW_SPECS = {
@@ -233,6 +276,9 @@ _VIEW_SPECS = {
     "recv_src": (torch.int32, lambda s: (s.recv_src_capacity,)),
     "expert_ids": (torch.int32, lambda s: (s.R, s.L)),
     "expert_usage_stats": (torch.int32, lambda s: (s.R, 2)),
+    "tok_dst": (torch.int32, lambda s: (s.R, s.T, s.K)),
+    "recv_src_tok": (torch.int32, lambda s: (s.tok_capacity,)),
+    "rank_tok_base": (torch.int64, lambda s: (s.R + 1,)),
 }
 
 
@@ -252,7 +298,9 @@ class EPLayout:
         off = (-self.workspace.data_ptr()) % 256
         self.ws = self.workspace[off:off + nbytes]
         self.h = ep_handle_create(self.params, self.ws)
-        self.recv_src_capacity = ep_handle_views(self.h).recv_src_capacity
+        v = ep_handle_views(self.h)
+        self.recv_src_capacity = v.recv_src_capacity
+        self.tok_capacity = v.tok_capacity
 
     def __del__(self):
         h = getattr(self, "h", None)
@@ -332,6 +380,53 @@ class EPLayout:
         db, _ = ep_recv_row_bytes(self.H, quant)
         cap = min(recv_data.numel() // db, y.numel() // self.H)
         ep_expert_identity(self.h, quant, recv_data, recv_scales, cap, mark_mod, y, stream)
+        return y
+
+    # ---------------------------------------------------------- per-rank layout
+
+    def token_layout(self, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
+                     active_mask: torch.Tensor | None = None, rows_capacity: int | None = None,
+                     stream=None, out=None):
+        """DeepEP per-rank receive layout; call after layout() with the same topk and
+        mask.  Returns (recv_topk_idx [cap, K] int64, recv_topk_weights [cap, K] f32),
+        written into ``out`` when given."""
+        dev = topk_idx.device
+        if out is not None:
+            ridx, rw = out
+            cap = ridx.shape[0] if rows_capacity is None else rows_capacity
+        else:
+            cap = self.tok_capacity if rows_capacity is None else rows_capacity
+            ridx = torch.empty((max(cap, 1), self.K), dtype=torch.int64, device=dev)
+            rw = torch.empty((max(cap, 1), self.K), dtype=torch.float32, device=dev)
+        m, dims = None, 0
+        if active_mask is not None:
+            m = active_mask.to(torch.uint8).contiguous()
+            dims = 1 if m.numel() == self.R * self.T else 2
+            self._tmask = m
+        ep_token_layout(self.h, topk_idx, topk_weights.contiguous(), m, dims, ridx, rw, cap, stream)
+        return ridx, rw
+
+    def token_rows(self, stream=None) -> list[int]:
+        return ep_handle_token_rows(self.h, self.R, stream)
+
+    def dispatch_tokens(self, x, quant, recv_data, recv_scales, stream=None, scales=None,
+                        scale_kind=EP_SCALES_NONE) -> None:
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        ep_dispatch_tokens(self.h, x, quant, scales, scale_kind, recv_data, recv_scales,
+                           recv_data.numel() // db, stream)
+
+    def combine_tokens(self, y, out, shared=None, rank_weights=None, out_weights=None, stream=None):
+        S = 0 if shared is None else shared.shape[1]
+        ep_combine_tokens(self.h, y, y.numel() // self.H, shared, S, out, rank_weights, out_weights,
+                          stream)
+        return out
+
+    def expert_identity_tokens(self, quant, recv_data, recv_scales, recv_topk_idx, recv_topk_weights,
+                               y, mark_mod: int = 0, stream=None):
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        cap = min(recv_data.numel() // db, y.numel() // self.H, recv_topk_idx.shape[0])
+        ep_expert_identity_tokens(self.h, quant, recv_data, recv_scales, recv_topk_idx,
+                                  recv_topk_weights, cap, mark_mod, y, stream)
         return y
 
 

@@ -138,6 +138,14 @@ typedef struct ep_layout_views {
     const int32_t* expert_ids;
     const int32_t* expert_usage_stats;
     int64_t recv_src_capacity;
+    /* per-rank receive layout (after ep_token_layout): tok_dst [R,T,K] rows
+     * of the token on its destination ranks in ascending rank order, -1
+     * padded; recv_src_tok [tok_capacity] source token of each row;
+     * rank_tok_base [R+1] first row of each rank. */
+    const int32_t* tok_dst;
+    const int32_t* recv_src_tok;
+    const int64_t* rank_tok_base;
+    int64_t tok_capacity;
 } ep_layout_views;
 
 /* Human-readable name of a status code (static storage; never NULL). */
@@ -278,6 +286,58 @@ ep_status ep_expert_identity(const ep_handle* handle, ep_quant_mode quant,
                              const void* recv_data, const void* recv_scales,
                              int64_t rows_capacity, int32_t mark_mod, void* y,
                              ep_stream_t stream);
+
+/* ---- DeepEP per-rank receive layout (one row per token and rank) -------- */
+
+/* Device.  The receive layout of DeepEP's Buffer.dispatch (Normal Mode API
+ * returns): rank j receives every token with an expert on j once, in (source
+ * rank, token) order, ranks back to back.  Writes recv_topk_idx [rows, K]
+ * (int64: the local expert id e - j*L of experts on the receiving rank, -1
+ * otherwise) and recv_topk_weights [rows, K] (float32: the token's weight for
+ * such an expert, 0 otherwise) for rows_capacity rows, and the handle's
+ * tok_dst / recv_src_tok / rank_tok_base (see ep_layout_views).  Uses the
+ * per-CTA token counts of the preceding ep_layout / ep_layout_masked on the
+ * same stream, which must have been given the same topk_idx and mask.
+ * topk_weights [R,T,K] float32 (device); active_mask as ep_layout_masked
+ * (NULL: none).  More rows than rows_capacity (or than R*T*min(R,K)) sets
+ * EP_ERR_CAPACITY. */
+ep_status ep_token_layout(ep_handle* handle, const int64_t* topk_idx, const float* topk_weights,
+                          const uint8_t* active_mask, int32_t mask_dims, int64_t* recv_topk_idx,
+                          float* recv_topk_weights, int64_t rows_capacity, ep_stream_t stream);
+
+/* Synchronises the stream, then copies rank_tok_base [R+1] (int64) to host
+ * memory: the per-rank layout's rows of rank j are [base[j], base[j+1]). */
+ep_status ep_handle_token_rows(const ep_handle* handle, int64_t* rank_tok_base_host,
+                               ep_stream_t stream);
+
+/* Device.  Dispatch into the per-rank layout: each token's row (encoded as
+ * for ep_dispatch_scaled; per-expert scales are not defined for it) is written
+ * once per destination rank.  Same layouts, capacity and errors. */
+ep_status ep_dispatch_tokens(const ep_handle* handle, const void* x, ep_quant_mode quant,
+                             const float* scales, ep_scale_kind scale_kind, void* recv_data,
+                             void* recv_scales, int64_t recv_rows_capacity, ep_stream_t stream);
+
+/* Device.  Combine of the per-rank layout (DeepEP Buffer.combine): each rank's
+ * expert stage has already weighted and summed its local experts, so
+ *   out[s,t,:] = bf16( sum over the token's rows, ascending rank, of y[row,:]
+ *                      + sum_q shared[s,q,t,:] ),
+ * float32 accumulation.  If rank_weights [y_rows_capacity, K] and
+ * out_weights [R,T,K] (float32) are both given, the reduced weights
+ * out_weights[n][k] = sum over the token's rows of rank_weights[row][k] are
+ * written too (DeepEP returns them); pass NULL for both to skip. */
+ep_status ep_combine_tokens(const ep_handle* handle, const void* y, int64_t y_rows_capacity,
+                            const void* shared, int32_t num_shared, void* out,
+                            const float* rank_weights, float* out_weights, ep_stream_t stream);
+
+/* Device.  Stand-in expert stage of the per-rank layout (tests, benchmarks):
+ * y[row] = bf16( sum_k (recv_topk_weights[row,k] * 2^-(l_k mod mark_mod)) *
+ * v ) over the row's local experts l_k (recv_topk_idx >= 0), slot order, where
+ * v is the row dequantised as for ep_expert_identity and rounded to bf16. */
+ep_status ep_expert_identity_tokens(const ep_handle* handle, ep_quant_mode quant,
+                                    const void* recv_data, const void* recv_scales,
+                                    const int64_t* recv_topk_idx, const float* recv_topk_weights,
+                                    int64_t rows_capacity, int32_t mark_mod, void* y,
+                                    ep_stream_t stream);
 
 /* Writable device arrays of one layout, for ep_layout_static_scratch.  Shapes
  * as in ep_layout_views; status is one int32 word (the sticky status word). */

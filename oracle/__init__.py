@@ -271,7 +271,7 @@ def dispatch(lay: Layout, x_bf16: np.ndarray, q: int, row_begin: int = 0,
              row_end: int | None = None) -> tuple[np.ndarray, np.ndarray]:
     """Receive rows [row_begin, row_end) as (data bytes [rows, db], scale bytes [rows, sb])."""
     N = lay.R * lay.T
-    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, np.shape(x_bf16)[-1])
     H = x.shape[1]
     if row_end is None:
         row_end = lay.rows
@@ -291,7 +291,7 @@ def dispatch_scaled(lay: Layout, x_bf16: np.ndarray, q: int, topk: np.ndarray,
     """Receive rows with input scales of a kind (S_SCALAR [1], S_CHANNEL [H],
     S_EXPERT [E, H]); quantModes 1-3 only."""
     N = lay.R * lay.T
-    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, np.shape(x_bf16)[-1])
     H = x.shape[1]
     if row_end is None:
         row_end = lay.rows
@@ -310,7 +310,7 @@ def dispatch_scaled(lay: Layout, x_bf16: np.ndarray, q: int, topk: np.ndarray,
 def dispatch_rows(lay: Layout, x_bf16: np.ndarray, q: int, rows: np.ndarray):
     """Selected receive rows, computed one by one through recv_src."""
     N = lay.R * lay.T
-    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, np.shape(x_bf16)[-1])
     H = x.shape[1]
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     db, sb = row_bytes(q, H)
@@ -456,7 +456,7 @@ def token_layout(R: int, T: int, E: int, K: int, topk: np.ndarray, w: np.ndarray
 def token_dispatch(tl: TokenLayout, x_bf16: np.ndarray, q: int):
     """Receive rows of the per-rank layout (the same scatter, onto tok_dst)."""
     N = tl.R * tl.T
-    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, -1)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(N, np.shape(x_bf16)[-1])
     H = x.shape[1]
     db, sb = row_bytes(q, H)
     data = np.zeros((tl.rows, db), np.uint8)

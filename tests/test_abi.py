@@ -106,6 +106,8 @@ def test_workspace_carving_is_aligned_and_disjoint():
         s = S()
         s.R, s.T, s.E, s.K, s.L = R, T, E, K, E // R
         s.recv_src_capacity = v.recv_src_capacity
+        s.tok_capacity = v.tok_capacity
+        assert v.tok_capacity == R * T * min(R, K)
         worst = R * T * K + E * (w.expert_alignment - 1)
         assert v.recv_src_capacity == (w.recv_capacity_rows or worst)
         spans = []
@@ -202,3 +204,17 @@ def test_row_bytes_new_modes():
     assert ep.ep_recv_row_bytes(7168, ep.EP_QUANT_FP8_E5M2_PER_GROUP) == (7168, 224)
     with pytest.raises(ep.EPError):
         ep.ep_recv_row_bytes(4160, ep.EP_QUANT_FP8_E4M3_PER_GROUP)
+
+
+def test_token_layout_validation():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C, D = 1 << 40, 1 << 41, 1 << 42, 1 << 43
+    assert L.ep_token_layout(h, A, None, None, 0, C, D, 10, None) == ep.EP_ERR_INVALID_ARG   # no weights
+    assert L.ep_token_layout(h, A, B, None, 0, None, D, 10, None) == ep.EP_ERR_INVALID_ARG   # no idx out
+    assert L.ep_token_layout(h, A, B, C, 5, C, D, 10, None) == ep.EP_ERR_INVALID_ARG        # mask dims
+    assert L.ep_dispatch_tokens(h, A, 2, C, 3, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED      # per-expert
+    assert L.ep_combine_tokens(h, A, 10, None, 0, B, C, None, None) == ep.EP_ERR_INVALID_ARG  # weights pair
+    assert L.ep_expert_identity_tokens(h, 0, A, None, None, B, 4, 0, C, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
