@@ -107,6 +107,8 @@ def _declare(lib):
     lib.oracle_token_layout.restype = i64
     lib.oracle_expert_token_rows.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp, vp, i32, vp]
     lib.oracle_reduce_token_weights.argtypes = [i64, i32, vp, vp, vp]
+    lib.oracle_dispatch_bytes.argtypes = [i32, i32, vp, vp, i64, i64, i64, vp]
+    lib.oracle_encode_row.argtypes = [i32, i32, vp, vp, vp]
     return lib
 
 
@@ -201,7 +203,11 @@ def encode_row(q: int, x_bf16: np.ndarray, smooth=None):
     db, sb = row_bytes(q, H)
     data = np.zeros(db, np.uint8)
     scale = np.zeros(max(sb, 1), np.uint8)
-    load().oracle_encode_row_scaled(q, H, _p(x), _p(_scale_arr(smooth, H)), _p(data), _p(scale))
+    if smooth is None:
+        load().oracle_encode_row(q, H, _p(x), _p(data), _p(scale))
+    else:
+        assert q in (Q_INT8_STATIC, Q_INT8, Q_FP8T_E4M3, Q_FP8T_E5M2, Q_FP8G_E4M3, Q_FP8G_E5M2)
+        load().oracle_encode_row_scaled(q, H, _p(x), _p(_scale_arr(smooth, H)), _p(data), _p(scale))
     return data, scale[:sb]
 
 
@@ -305,6 +311,37 @@ def dispatch_scaled(lay: Layout, x_bf16: np.ndarray, q: int, topk: np.ndarray,
     load().oracle_dispatch_scaled(N, lay.K, H, q, _p(dr), _p(tk), _p(x), _p(sc), kind, row_begin,
                                   row_end, _p(data), _p(scl) if sb else None)
     return data, scl
+
+
+def dispatch_bytes(lay, src_rows: np.ndarray, rows: int | None = None) -> np.ndarray:
+    """Scatter of already-encoded source rows [N, nbytes] (uint8) onto the
+    receive rows of a layout (lay.dst_row, or a TokenLayout's tok_dst); rows
+    that no entry reaches are zero.  rows defaults to the layout's row count."""
+    N = lay.R * lay.T
+    src = np.ascontiguousarray(src_rows, dtype=np.uint8).reshape(N, -1) if N else \
+        np.zeros((0, np.shape(src_rows)[-1]), np.uint8)
+    nb = src.shape[1]
+    dst = lay.tok_dst if hasattr(lay, "tok_dst") else lay.dst_row
+    if rows is None:
+        rows = lay.rows
+    out = np.zeros((rows, nb), np.uint8)
+    dr = np.ascontiguousarray(dst.reshape(-1), dtype=np.int32)
+    load().oracle_dispatch_bytes(N, lay.K, _p(dr), _p(src), nb, 0, rows, _p(out))
+    return out
+
+
+def transpose_scales(scales_rows: np.ndarray, capacity: int, elem_bytes: int) -> np.ndarray:
+    """Row-major receive scales [rows, nb * elem_bytes] (uint8) rearranged into
+    the block-major layout of MAX ep_dispatch's output_scales, shape
+    (hidden // block_size, max_recv_tokens): element b of row r lands at
+    [b, r]; columns past the last row are zero.  Returned as uint8
+    [nb, capacity * elem_bytes]."""
+    s = np.ascontiguousarray(scales_rows, dtype=np.uint8)
+    rows = s.shape[0]
+    nb = s.shape[1] // elem_bytes
+    out = np.zeros((nb, capacity, elem_bytes), np.uint8)
+    out[:, :rows, :] = s.reshape(rows, nb, elem_bytes).transpose(1, 0, 2)
+    return out.reshape(nb, capacity * elem_bytes)
 
 
 def dispatch_rows(lay: Layout, x_bf16: np.ndarray, q: int, rows: np.ndarray):

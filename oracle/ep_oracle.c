@@ -601,6 +601,22 @@ void oracle_dispatch(int N, int K, int H, int q, const int32_t* dst_row,
     free(tmp_s);
 }
 
+/* Dispatch of rows that are already encoded (DeepEP "Normal Mode API",
+ * Quantization: x passed as a (data, scale) tuple): each source row is a fixed
+ * number of bytes and moves unchanged.  Every valid entry (n, k) receives
+ * src row n at dst_row[n*K+k]; rows no entry reaches (padding) are zero.  Called
+ * once for the data rows and once for the scale rows. */
+void oracle_dispatch_bytes(int N, int K, const int32_t* dst_row, const uint8_t* src, int64_t row_bytes,
+                           int64_t row_begin, int64_t row_end, uint8_t* out) {
+    memset(out, 0, (size_t)((row_end - row_begin) * row_bytes));
+    for (int64_t n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) {
+            int64_t d = dst_row[n * K + k];
+            if (d < row_begin || d >= row_end) continue;
+            memcpy(out + (d - row_begin) * row_bytes, src + n * row_bytes, (size_t)row_bytes);
+        }
+}
+
 /* Dispatch with input scales (quantModes 1-3): as oracle_dispatch, but each
  * entry's row is encoded with the scale row that applies to it: the scalar
  * scale[0] for every element (S_SCALAR), the shared row scale[0..H)

@@ -14,6 +14,7 @@ import pytest
 
 import oracle
 import test_oracle_dispatch_combine as tdc
+import test_oracle_formats as tfm
 import test_oracle_layout as tl
 import test_oracle_quant as tq
 import test_oracle_quant_ext as tqx
@@ -63,6 +64,11 @@ MUTANTS = {
                                    "recv_topk_weights[row * K + k] = w[n * K + k];"),
     "token_reduce_skips_last_row": ("            for (int i = 0; i < K; ++i) {\n                int32_t r = tok_dst[n * K + i];",
                                     "            for (int i = 0; i < K - 1; ++i) {\n                int32_t r = tok_dst[n * K + i];"),
+    "bytes_source_taken_at_destination": (
+        "memcpy(out + (d - row_begin) * row_bytes, src + n * row_bytes, (size_t)row_bytes);",
+        "memcpy(out + (d - row_begin) * row_bytes, src + d * row_bytes, (size_t)row_bytes);"),
+    "bytes_first_slot_only": ("        for (int k = 0; k < K; ++k) {\n            int64_t d = dst_row[n * K + k];\n            if (d < row_begin || d >= row_end) continue;\n            memcpy(out + (d - row_begin) * row_bytes, src + n",
+                              "        for (int k = 0; k < 1; ++k) {\n            int64_t d = dst_row[n * K + k];\n            if (d < row_begin || d >= row_end) continue;\n            memcpy(out + (d - row_begin) * row_bytes, src + n"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -94,6 +100,7 @@ def pins():
     cases += [lambda s=s: ttl.test_random_small_against_brute_force(s) for s in range(6)]
     cases += [lambda: ttl.test_combine_through_rank_expert_stage_closed_form(2, 24, 4),
               ttl.test_reduced_weights_equal_original_for_valid_entries]
+    cases += [lambda s=s: tfm.test_dispatch_bytes_brute_force(s) for s in range(4)]
     return cases
 
 
