@@ -38,23 +38,32 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s vs GB300 peak, 1 GPU"
-# key -> (workload index, quant mode, input-scale kind, xActiveMask dims, receive layout)
+# key -> (workload index, quant mode, input-scale kind, xActiveMask dims, receive layout,
+#         format)
 # receive layout "expert": one row per (token, expert), grouped per expert (MAX);
 # "rank": one row per (token, destination rank) (DeepEP).
-WORKLOAD_KEYS = {"1": (1, 0, 0, 0, "expert"), "2": (2, 0, 0, 0, "expert"),
-                 "3": (3, 2, 0, 0, "expert"), "4a": (4, 4, 0, 0, "expert"),
-                 "4b": (4, 6, 0, 0, "expert"), "5": (5, 0, 0, 0, "expert"),
+# format "": bf16 input, row-major scales; "pre": pre-encoded (data, scale) rows
+# moved unchanged (DeepEP tuple input); "bm": block-major scales (MAX output_scales).
+WORKLOAD_KEYS = {"1": (1, 0, 0, 0, "expert", ""), "2": (2, 0, 0, 0, "expert", ""),
+                 "3": (3, 2, 0, 0, "expert", ""), "4a": (4, 4, 0, 0, "expert", ""),
+                 "4b": (4, 6, 0, 0, "expert", ""), "5": (5, 0, 0, 0, "expert", ""),
                  # further CANN quant modes and xActiveMask on the same shapes
-                 "4t": (4, 7, 0, 0, "expert"), "4g": (4, 9, 0, 0, "expert"),
-                 "3s": (3, 1, 2, 0, "expert"), "3e": (3, 2, 3, 0, "expert"),
-                 "5m": (5, 0, 0, 2, "expert"),
+                 "4t": (4, 7, 0, 0, "expert", ""), "4g": (4, 9, 0, 0, "expert", ""),
+                 "3s": (3, 1, 2, 0, "expert", ""), "3e": (3, 2, 3, 0, "expert", ""),
+                 "5m": (5, 0, 0, 2, "expert", ""),
                  # the DeepEP per-rank receive layout
-                 "2r": (2, 0, 0, 0, "rank"), "4r": (4, 4, 0, 0, "rank")}
+                 "2r": (2, 0, 0, 0, "rank", ""), "4r": (4, 4, 0, 0, "rank", ""),
+                 # alternate formats
+                 "4p": (4, 4, 0, 0, "expert", "pre"), "4x": (4, 4, 0, 0, "expert", "bm")}
+FORMAT = {"": "bf16 input, row-major scales",
+          "pre": "pre-encoded (data, scale) rows moved unchanged",
+          "bm": "block-major scales (blocks, capacity)"}
 QNAME = {0: "none", 1: "int8_static", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2",
          6: "mxfp4_e2m1", 7: "fp8_e4m3_per_token", 8: "fp8_e5m2_per_token",
          9: "fp8_e4m3_per_group128", 10: "fp8_e5m2_per_group128"}
 SCALE_KIND = {0: "none", 1: "scalar", 2: "per_channel", 3: "per_expert"}
 SAMPLE_NOTE = " (input scales and xActiveMask are not applied in the oracle sample)"
+FORMAT_NOTE = " (the oracle sample runs the fused bf16-input, row-major path of the same mode)"
 KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "layout": "layout.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
@@ -208,14 +217,17 @@ def make_inputs(w, device):
     return topk, wts, x_dev, sh_dev
 
 
-def algorithmic_bytes(w, quant, rows, V, per_rank=False):
+def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt=""):
     """Bytes each kernel must move (reads + writes).  Expert layout: V gathered
     rows in combine; per-rank layout: every receive row is gathered once (unit
-    weights, no weight reads)."""
+    weights, no weight reads).  Pre-encoded input: the encoded rows are read
+    instead of bf16 ones, plus recv_src for the scale gather."""
     from combine_ep_layout_03_gb300 import ep
     db, sb = ep.ep_recv_row_bytes(w.H, quant)
     N, H, K, S = w.N, w.H, w.K, w.num_shared
     disp = N * H * 2 + N * K * 4 + rows * (db + sb)
+    if fmt == "pre":
+        disp = N * (db + sb) + N * K * 4 + rows * (db + sb) + (rows * 4 if sb else 0)
     lay = N * K * 8 * 3 + N * K * 4 + rows * 4 + N * w.R
     if per_rank:
         comb = rows * H * 2 + N * K * 4 + S * N * H * 2 + N * H * 2
@@ -225,7 +237,8 @@ def algorithmic_bytes(w, quant, rows, V, per_rank=False):
     return {"layout": lay, "dispatch": disp, "combine": comb}
 
 
-def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_layout="expert"):
+def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_layout="expert",
+             fmt=""):
     from combine_ep_layout_03_gb300 import ep, synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -249,14 +262,25 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         rows = int(lay.recv_rows()[-1])
     V = int((topk >= 0).sum()) if mask_dev is None else None
     data, scales = lay.alloc_recv(quant, max(rows, 1), device=dev)
+    scales_rm = scales
+    if fmt == "bm":
+        data, scales = lay.alloc_recv_block_major(quant, max(rows, 1), device=dev)
+    xs_dev = None
+    x_bf16 = x_dev
+    if fmt == "pre":
+        db_, sb_ = ep.ep_recv_row_bytes(w.H, quant)
+        x_dev, xs_dev = synth.gen_encoded_rows_device(w, db_, sb_, device=dev)
 
     def do_layout(topk_t, w_t, s=None):
         lay.layout(topk_t, s, active_mask=mask_dev)
         if per_rank:
             lay.token_layout(topk_t, w_t, active_mask=mask_dev, stream=s, out=(ridx, rw))
 
-    def do_dispatch(x_t, s=None):
-        if per_rank:
+    def do_dispatch(x_t, s=None, xs_t=None):
+        if fmt:
+            lay.dispatch_ex(x_t, quant, data, scales, s, x_scales=xs_t, per_rank=per_rank,
+                            pre_encoded=fmt == "pre", block_major=fmt == "bm")
+        elif per_rank:
             lay.dispatch_tokens(x_t, quant, data, scales, s, scales=sc_dev, scale_kind=kind)
         else:
             lay.dispatch(x_t, quant, data, scales, s, scales=sc_dev, scale_kind=kind)
@@ -267,8 +291,13 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         else:
             lay.combine(y, w_t, out_t, sh_t, s)
 
-    if quant == 0:
+    if quant == 0 and not fmt:
         y = data.view(torch.bfloat16).view(-1, w.H)
+    elif fmt:
+        # expert outputs from the fused row-major path of the same bf16 x
+        lay.dispatch(x_bf16, quant, data, scales_rm, None, scales=sc_dev, scale_kind=kind)
+        y = torch.empty((max(rows, 1), w.H), dtype=torch.bfloat16, device=dev)
+        lay.expert_identity(quant, data, scales_rm, y)
     else:
         do_dispatch(x_dev)
         y = torch.empty((max(rows, 1), w.H), dtype=torch.bfloat16, device=dev)
@@ -285,7 +314,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         do_layout(topk_dev, w_dev)
         if ev is not None:
             ev[1].record(stream)
-        do_dispatch(x_dev)
+        do_dispatch(x_dev, None, xs_dev)
         if ev is not None:
             ev[2].record(stream)
         do_combine(w_dev, out, sh_dev)
@@ -331,16 +360,20 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
             h.copy_(t)
             return h
         x_host = pinned_like(x_dev)
+        xs_host = None if xs_dev is None else pinned_like(xs_dev)
         topk_host = torch.from_numpy(topk).pin_memory()
         w_host = torch.from_numpy(wts).pin_memory()
         sh_host = None if sh_dev is None else pinned_like(sh_dev)
         out_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-        slots = [dict(x=x_dev, topk=topk_dev, w=w_dev, sh=sh_dev, out=out)]
-        slots.append(dict(x=torch.empty_like(x_dev), topk=torch.empty_like(topk_dev),
+        slots = [dict(x=x_dev, xs=xs_dev, topk=topk_dev, w=w_dev, sh=sh_dev, out=out)]
+        slots.append(dict(x=torch.empty_like(x_dev),
+                          xs=None if xs_dev is None else torch.empty_like(xs_dev),
+                          topk=torch.empty_like(topk_dev),
                           w=torch.empty_like(w_dev),
                           sh=None if sh_dev is None else torch.empty_like(sh_dev),
                           out=torch.empty_like(out)))
-        h2d = x_host.numel() * 2 + topk_host.numel() * 8 + w_host.numel() * 4
+        h2d = x_host.numel() * x_host.element_size() + topk_host.numel() * 8 + w_host.numel() * 4
+        h2d += 0 if xs_host is None else xs_host.numel()
         h2d += 0 if sh_host is None else sh_host.numel() * 2
         d2h = out.numel() * 2
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -356,6 +389,8 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
                     if i >= 2:
                         s_in.wait_event(ev_k[i - 2])      # slot's inputs no longer read
                     sl["x"].copy_(x_host, non_blocking=True)
+                    if xs_host is not None:
+                        sl["xs"].copy_(xs_host, non_blocking=True)
                     sl["topk"].copy_(topk_host, non_blocking=True)
                     sl["w"].copy_(w_host, non_blocking=True)
                     if sh_host is not None:
@@ -365,7 +400,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
                 if i >= 2:
                     s_k.wait_event(ev_out[i - 2])         # slot's output already read back
                 do_layout(sl["topk"], sl["w"], s_k)
-                do_dispatch(sl["x"], s_k)
+                do_dispatch(sl["x"], s_k, sl["xs"])
                 do_combine(sl["w"], sl["out"], sl["sh"], s_k)
                 ev_k[i].record(s_k)
                 with torch.cuda.stream(s_out):
@@ -389,14 +424,14 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         e2e_ms = s2.elapsed_time(t2) / k2
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h, "steps": k2}
         assert lay.status() == ep.EP_OK
-        if quant == 0:
+        if quant == 0 and not fmt:
             # the copied-back output of the last step equals the device-resident result
             assert torch.equal(out_host[(k2 - 1) % 2].to(dev), out)
 
     clocks = sampler.summary(t_timed0, t_timed1, t_warm0)
-    bytes_ = algorithmic_bytes(w, quant, rows, V, per_rank)
+    bytes_ = algorithmic_bytes(w, quant, rows, V, per_rank, fmt)
     return dict(total_ms=total_ms, phase=phase, e2e=e2e, clocks=clocks, bytes=bytes_, rows=rows,
-                V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_dev, sh_dev=sh_dev)
+                V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_bf16, sh_dev=sh_dev)
 
 
 # --------------------------------------------------------------------- CPU oracle
@@ -459,7 +494,7 @@ def host_shared_lead(sh_dev, w, ranks=2):
 
 def workload_config(w, quant, key, kind=0, mask_dims=0):
     return {"workload": f"ep_layout_dispatch_combine[{key}] " + w.name,
-            "receive_layout": WORKLOAD_KEYS[key][4],
+            "receive_layout": WORKLOAD_KEYS[key][4], "format": FORMAT[WORKLOAD_KEYS[key][5]],
             "input_scales": SCALE_KIND[kind], "active_mask_dims": mask_dims,
             "R": w.R, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "alpha": w.alpha,
             "routing": w.routing, "drop_p": w.drop_p, "num_shared": w.num_shared,
@@ -473,7 +508,7 @@ def main(argv=None):
     args = parse_args(argv)
     rank, local_rank, world = dist_env()
     from combine_ep_layout_03_gb300 import synth
-    idx, quant, kind, mask_dims, recv_layout = WORKLOAD_KEYS[args.workload]
+    idx, quant, kind, mask_dims, recv_layout, fmt = WORKLOAD_KEYS[args.workload]
     w = synth.WORKLOADS[idx]
     if args.tokens_per_rank:
         w = w.with_(T=args.tokens_per_rank)
@@ -486,7 +521,7 @@ def main(argv=None):
     if world > 1:
         import datetime
         torch.distributed.init_process_group("gloo", timeout=datetime.timedelta(minutes=10))
-    res = run_ours(args, w, quant, rank, local_rank, world, kind, mask_dims, recv_layout)
+    res = run_ours(args, w, quant, rank, local_rank, world, kind, mask_dims, recv_layout, fmt)
     K = args.steps
     res["total_ms"], e2e_ms = max_over_ranks(
         [res["total_ms"], res["e2e"]["ms"] if res["e2e"] else 0.0], world)
@@ -512,7 +547,7 @@ def main(argv=None):
         sh0 = host_shared_lead(res["sh_dev"], w)
         v, desc, spent, n = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget)
         cpu = {"value": round(v, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": desc + SAMPLE_NOTE * bool(kind or mask_dims)}
+               "sample": desc + SAMPLE_NOTE * bool(kind or mask_dims) + FORMAT_NOTE * bool(fmt)}
 
     e2e = None
     if res["e2e"]:
@@ -526,7 +561,8 @@ def main(argv=None):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if quant == 0 else f"bf16->{QNAME[quant]}",
+        "dtype": f"u8 (pre-encoded {QNAME[quant]} rows)" if fmt == "pre" else
+                 ("bf16" if quant == 0 else f"bf16->{QNAME[quant]}"),
         "data": "synthetic (seeded: x ~ N(0,1) rounded to bf16, routing and softmax weights per "
                 "the workload's recipe; identity experts)",
         "config": workload_config(w, quant, args.workload, kind, mask_dims),

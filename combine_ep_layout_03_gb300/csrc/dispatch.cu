@@ -23,9 +23,18 @@
 // to its K destination rows by cp.async.bulk stores, one bulk group per token,
 // and a stage is refilled once cp.async.bulk.wait_group.read shows the stores
 // issued kTmaLag tokens earlier have read it.  Warps 1..3 of the CTA zero the
-// padding rows meanwhile.
+// padding rows meanwhile.  The same kernel moves pre-encoded rows (DeepEP
+// "Normal Mode API", Quantization: x given as a (data, scale) tuple): the
+// source row is then any fixed number of bytes, and warps 1..3 also gather the
+// scale rows per receive row.
+//
+// Scales can be written block-major (Modular MAX "EPBatchManager",
+// ep_dispatch output_scales of shape (hidden // block_size, max_recv_tokens)):
+// element b of receive row r at b * capacity + r.
 #include "ep_internal.cuh"
 #include "tma.cuh"
+
+#include <type_traits>
 
 namespace {
 
@@ -97,6 +106,32 @@ struct QTraits {
     static constexpr int VB = (Q == M_E2M1) ? 4 : 8;  // code bytes per 8 elements
 };
 
+// Address of scale element b (scale_elem bytes) of receive row r, row-major or
+// block-major (MAX output_scales: element b of row r at b * cap + r).
+__device__ __forceinline__ uint8_t* scale_at(const DispatchArgs& a, int64_t r, int b) {
+    return a.scales_t ? a.scales + ((int64_t)b * a.cap + r) * a.scale_elem
+                      : a.scales + r * a.scale_bytes + (int64_t)b * a.scale_elem;
+}
+
+// Zero the scale entries of padding rows [r0, r1), threads part..nparts.
+__device__ void zero_scale_rows(const DispatchArgs& a, int64_t r0, int64_t r1, int part, int nparts) {
+    // with staged scales the gather pass writes the padding rows' zeros
+    if (r1 <= r0 || !a.scale_bytes || a.src_scales) return;
+    if (!a.scales_t) {
+        const int64_t sbytes = (r1 - r0) * a.scale_bytes;
+        uint8_t* sb = a.scales + r0 * a.scale_bytes;
+        for (int64_t i = part; i < sbytes; i += nparts) sb[i] = 0;
+        return;
+    }
+    const int64_t n = r1 - r0;
+    const int64_t cnt = n * (a.scale_bytes / a.scale_elem);
+    for (int64_t i = part; i < cnt; i += nparts) {   // consecutive threads: consecutive rows
+        uint8_t* p = scale_at(a, r0 + i % n, (int)(i / n));
+        if (a.scale_elem == 4) *reinterpret_cast<uint32_t*>(p) = 0u;
+        else *p = 0;
+    }
+}
+
 // Zero one padding row region [r0, r1) of data and scales with the whole CTA.
 __device__ void zero_rows(const DispatchArgs& a, int64_t r0, int64_t r1) {
     if (r1 <= r0) return;
@@ -109,11 +144,7 @@ __device__ void zero_rows(const DispatchArgs& a, int64_t r0, int64_t r1) {
         for (int64_t i = threadIdx.x; i < nbytes / 8; i += blockDim.x)
             st_v2(base + i * 8, make_uint2(0, 0));
     }
-    if (a.scale_bytes) {
-        const int64_t sbytes = (r1 - r0) * a.scale_bytes;
-        uint8_t* sb = a.scales + r0 * a.scale_bytes;
-        for (int64_t i = threadIdx.x; i < sbytes; i += blockDim.x) sb[i] = 0;
-    }
+    zero_scale_rows(a, r0, r1, threadIdx.x, blockDim.x);
 }
 
 // Multiply the row's floats by the input scales (quantModes 1-3).
@@ -289,6 +320,8 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
         }
         constexpr int VB = TR::VB;
         const bool stage_scales = BULK && scale_bulk;
+        // block-major scales: the token's scale row goes once to its staging row
+        const bool to_src = (TR::mx || TR::group) && a.src_scales != nullptr;
 
         if constexpr (BULK) {
             uint8_t* stg = qstage + (size_t)(j & 1) * stage_bytes;
@@ -313,11 +346,28 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
                     const int d = sdst[k];
                     if (d < 0) continue;
                     bulk_store(a.data + (int64_t)d * a.row_bytes, stg, (uint32_t)a.row_bytes);
-                    if (stage_scales)
+                    if (stage_scales && !to_src)
                         bulk_store(a.scales + (int64_t)d * a.scale_bytes, stg + scale_off,
                                    (uint32_t)a.scale_bytes);
                 }
+                if (stage_scales && to_src)
+                    bulk_store(a.src_scales + w * a.scale_bytes, stg + scale_off, (uint32_t)a.scale_bytes);
                 bulk_commit();
+            }
+        }
+        if constexpr (TR::mx || TR::group) {
+            if (to_src && !stage_scales) {
+                uint8_t* srow = a.src_scales + w * a.scale_bytes;
+#pragma unroll
+                for (int u = 0; u < VPT; ++u) {
+                    const int vi = u * NT + tid;
+                    if (vi >= a.nvec) continue;
+                    if constexpr (TR::mx) {
+                        if ((vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
+                    } else {
+                        if ((vi & 15) == 0) reinterpret_cast<float*>(srow)[vi >> 4] = ginv[u];
+                    }
+                }
             }
         }
         for (int k = 0; k < a.K; ++k) {
@@ -326,16 +376,15 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
             if constexpr (TR::token) {
                 if (tid == 0) reinterpret_cast<float*>(a.scales)[d] = inv;
             } else if constexpr (TR::mx || TR::group) {
-                if (!stage_scales) {
-                    uint8_t* srow = a.scales + (int64_t)d * a.scale_bytes;
+                if (!stage_scales && !to_src) {
 #pragma unroll
                     for (int u = 0; u < VPT; ++u) {
                         const int vi = u * NT + tid;
                         if (vi >= a.nvec) continue;
                         if constexpr (TR::mx) {
-                            if ((vi & 3) == 0) srow[vi >> 2] = (uint8_t)sbyte[u];
+                            if ((vi & 3) == 0) *scale_at(a, d, vi >> 2) = (uint8_t)sbyte[u];
                         } else {
-                            if ((vi & 15) == 0) reinterpret_cast<float*>(srow)[vi >> 4] = ginv[u];
+                            if ((vi & 15) == 0) *reinterpret_cast<float*>(scale_at(a, d, vi >> 4)) = ginv[u];
                         }
                     }
                 }
@@ -447,7 +496,7 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 if (vi < a.nvec) {
                     st_v2(row + (int64_t)vi * 8, make_uint2(packed[0], packed[1]));
                     if constexpr (TR::group) {
-                        if ((vi & 15) == 0) reinterpret_cast<float*>(srow)[vi >> 4] = gi;
+                        if ((vi & 15) == 0) *reinterpret_cast<float*>(scale_at(a, d, vi >> 4)) = gi;
                     }
                 }
             }
@@ -472,6 +521,81 @@ __device__ void zero_rows_part(const DispatchArgs& a, int64_t r0, int64_t r1, in
     const int64_t nbytes = (r1 - r0) * a.row_bytes;
     uint8_t* base = a.data + r0 * a.row_bytes;
     for (int64_t i = part; i < nbytes / 16; i += nparts) st_v4(base + i * 16, make_uint4(0, 0, 0, 0));
+}
+
+// Scale rows gathered per receive row from per-source-token rows src
+// [N][scale_bytes] (pre-encoded input, or the fused path's staging rows):
+// element c of receive row r takes element c of src row recv_src[r], and 0 for
+// a padding row.  Block-major: one receive row per thread, so for every block
+// b a warp stores 32 consecutive rows (one 32-byte run); the thread reads its
+// source row 16 bytes at a time when VEC.  Row-major: one receive row per
+// warp, lanes across the row.  The source rows are small and stay in L2.
+template <int ES, bool VEC>
+__global__ void __launch_bounds__(256) scale_gather_kernel(DispatchArgs a, const uint8_t* src) {
+    using T = typename std::conditional<ES == 4, uint32_t, uint8_t>::type;
+    const int64_t total = a.expert_base[a.E];
+    if (total > a.cap) return;   // the dispatch kernel has reported EP_ERR_CAPACITY
+    const int nb = a.scale_bytes / ES;
+    const T* s = reinterpret_cast<const T*>(src);
+    T* out = reinterpret_cast<T*>(a.scales);
+    if (a.scales_t) {
+        const int64_t step = (int64_t)gridDim.x * blockDim.x;
+        for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < total; r += step) {
+            const int sr = a.recv_src[r];
+            T* o = out + r;
+            if (sr < 0) {
+                for (int b = 0; b < nb; ++b) o[(int64_t)b * a.cap] = T(0);
+                continue;
+            }
+            if constexpr (VEC) {
+                constexpr int PER = 16 / ES;
+                const uint4* srow = reinterpret_cast<const uint4*>(src + (int64_t)sr * a.scale_bytes);
+                for (int v = 0; v < nb / PER; ++v) {
+                    const uint4 q = __ldg(srow + v);
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int j = 0; j < PER; ++j) {
+                        T e;
+                        if constexpr (ES == 4) e = w[j];
+                        else e = (T)(w[j >> 2] >> (8 * (j & 3)));
+                        o[(int64_t)(v * PER + j) * a.cap] = e;
+                    }
+                }
+            } else {
+                const T* srow = s + (int64_t)sr * nb;
+#pragma unroll 4
+                for (int b = 0; b < nb; ++b) o[(int64_t)b * a.cap] = __ldg(srow + b);
+            }
+        }
+    } else {
+        const int lane = threadIdx.x & 31;
+        const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+        for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total; r += warps) {
+            const int sr = a.recv_src[r];
+            T* o = out + r * nb;
+            const T* srow = s + (int64_t)(sr < 0 ? 0 : sr) * nb;
+            for (int c = lane; c < nb; c += 32) o[c] = sr >= 0 ? __ldg(srow + c) : T(0);
+        }
+    }
+}
+
+cudaError_t launch_scale_gather(const ep_handle* h, const DispatchArgs& a, const uint8_t* src,
+                                cudaStream_t st) {
+    // element size: the mode's unit when block-major; 4-byte words when row-major and possible
+    const bool words = a.scales_t ? a.scale_elem == 4
+                                  : (a.scale_bytes % 4 == 0 && (uintptr_t)src % 4 == 0 &&
+                                     (uintptr_t)a.scales % 4 == 0);
+    // 16-byte source reads of whole rows (block-major)
+    const bool vec = a.scales_t && a.scale_bytes % 16 == 0 && (uintptr_t)src % 16 == 0;
+    const int grid = h->num_sms * 8;
+    if (words) {
+        if (vec) scale_gather_kernel<4, true><<<grid, 256, 0, st>>>(a, src);
+        else scale_gather_kernel<4, false><<<grid, 256, 0, st>>>(a, src);
+    } else {
+        if (vec) scale_gather_kernel<1, true><<<grid, 256, 0, st>>>(a, src);
+        else scale_gather_kernel<1, false><<<grid, 256, 0, st>>>(a, src);
+    }
+    return cudaGetLastError();
 }
 
 __global__ void __launch_bounds__(128)
@@ -513,7 +637,8 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
         const int64_t b1 = ((first + a.K) * 4 + 15) & ~(int64_t)15;
         const uint32_t wbytes = (uint32_t)(b1 - b0);
         mbar_arrive_expect_tx(&full[s], row + wbytes);
-        bulk_load(stages + (size_t)s * stage_bytes, a.x + n * a.H, row, &full[s]);
+        bulk_load(stages + (size_t)s * stage_bytes, reinterpret_cast<const uint8_t*>(a.x) + n * row, row,
+                  &full[s]);
         bulk_load(sdst + s * kDstSlotInts, dst_bytes + b0, wbytes, &full[s]);
     };
     const int64_t pro = cnt < nstages ? cnt : nstages;
@@ -606,17 +731,16 @@ cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st)
     // bulk stores need 16-byte rows (the receive buffer itself is 16-byte aligned)
     const bool bulk = (a.row_bytes % 16) == 0;
     if (!bulk) return launch_q_impl<Q, false>(h, a, nt, 0, 0, 0, st);
-    const int scale_bulk = ((QTraits<Q>::mx || QTraits<Q>::group) && a.scale_bytes % 16 == 0 &&
-                            ((uintptr_t)a.scales % 16) == 0) ? 1 : 0;
+    const uint8_t* scale_dst = a.src_scales ? a.src_scales : a.scales;
+    const int scale_bulk = ((QTraits<Q>::mx || QTraits<Q>::group) && (!a.scales_t || a.src_scales) &&
+                            a.scale_bytes % 16 == 0 && ((uintptr_t)scale_dst % 16) == 0) ? 1 : 0;
     const int scale_off = (a.row_bytes + 15) / 16 * 16;
     int stage_bytes = scale_off + (scale_bulk ? (a.scale_bytes + 15) / 16 * 16 : 0);
     stage_bytes = (stage_bytes + 127) / 128 * 128;
     return launch_q_impl<Q, true>(h, a, nt, stage_bytes, scale_off, scale_bulk, st);
 }
 
-}  // namespace
-
-cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
+cudaError_t launch_dispatch_encode(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
     switch (quant) {
         case M_NONE: return launch_bf16_tma(h, a, st);
         case M_INT8S: return launch_q<M_INT8S>(h, a, st);
@@ -630,4 +754,18 @@ cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant
         case M_FP8G_E5M2: return launch_q<M_FP8G_E5M2>(h, a, st);
         default: return cudaErrorInvalidValue;
     }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_bytes(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
+    cudaError_t err = launch_bf16_tma(h, a, st);
+    if (err == cudaSuccess && a.scale_bytes && a.xs) err = launch_scale_gather(h, a, a.xs, st);
+    return err;
+}
+
+cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
+    cudaError_t err = launch_dispatch_encode(h, a, quant, st);
+    if (err == cudaSuccess && a.src_scales) err = launch_scale_gather(h, a, a.src_scales, st);
+    return err;
 }

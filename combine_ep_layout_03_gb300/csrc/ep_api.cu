@@ -60,7 +60,7 @@ int64_t tok_cap_of(const ep_params* p) {
 struct Carve {
     size_t status, blk_hist, blk_rank, cnt, itr, ntpr, recv_cnt, aligned, expert_start,
         rank_base, expert_base, src_prefix, dst_row, recv_src, expert_ids, usage,
-        tok_dst, recv_src_tok, tok_blk, tok_total, tok_base, tok_meta, total;
+        tok_dst, recv_src_tok, tok_blk, tok_total, tok_base, tok_meta, src_scales, total;
 };
 
 Carve carve_of(const ep_params* p) {
@@ -92,6 +92,10 @@ Carve carve_of(const ep_params* p) {
     c.tok_total = take(sizeof(int32_t) * (size_t)R);
     c.tok_base = take(sizeof(int64_t) * (size_t)(R + 1));
     c.tok_meta = take(sizeof(int32_t) * 4);
+    // the largest scale row of any mode: H/32 bytes (MX e8m0, or one float32
+    // per 128 elements), at least the 4 bytes of the per-token modes
+    const int64_t max_sb = p->hidden / 32 > 4 ? p->hidden / 32 : 4;
+    c.src_scales = take((size_t)(N * max_sb));
     c.total = off;
     return c;
 }
@@ -211,6 +215,7 @@ ep_status ep_handle_create(const ep_params* p, void* workspace, size_t workspace
     h->tok_total = (int32_t*)(w + c.tok_total);
     h->tok_base = (int64_t*)(w + c.tok_base);
     h->tok_meta = (int32_t*)(w + c.tok_meta);
+    h->src_scales = (uint8_t*)(w + c.src_scales);
     *out = h;
     return EP_OK;
 }
@@ -292,10 +297,13 @@ namespace {
 // targets the per-rank layout (tok_dst, one segment without padding).
 ep_status dispatch_impl(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
                         ep_scale_kind kind, void* recv_data, void* recv_scales, int64_t cap,
-                        ep_stream_t stream, bool tokens) {
+                        ep_stream_t stream, bool tokens, const void* x_scales = nullptr,
+                        uint32_t flags = 0) {
     ep_handle* h = const_cast<ep_handle*>(hc);
     if (!h) return EP_ERR_INVALID_ARG;
     if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    const bool pre = (flags & EP_DISPATCH_PRE_ENCODED) != 0;
+    const bool block_major = (flags & EP_DISPATCH_SCALES_BLOCK_MAJOR) != 0;
     if (is_mx(q) && h->H % 32 != 0) return EP_ERR_INVALID_ARG;
     if (is_group(q) && h->H % 128 != 0) return EP_ERR_INVALID_ARG;
     if (kind < EP_SCALES_NONE || kind > EP_SCALES_PER_EXPERT) return EP_ERR_INVALID_ARG;
@@ -311,6 +319,14 @@ ep_status dispatch_impl(const ep_handle* hc, const void* x, ep_quant_mode q, con
     ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);
     if (s != EP_OK) return s;
     if (sb > 0 && cap > 0 && (!recv_scales || !aligned_to(recv_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (pre) {
+        if (kind != EP_SCALES_NONE) return EP_ERR_INVALID_ARG;
+        if (db % 16 != 0) return EP_ERR_UNSUPPORTED;
+        if (sb == 0 && x_scales) return EP_ERR_INVALID_ARG;
+        if (sb > 0 && h->N > 0 && (!x_scales || !aligned_to(x_scales, 4))) return EP_ERR_INVALID_ARG;
+    } else if (x_scales) {
+        return EP_ERR_INVALID_ARG;
+    }
     if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
     DispatchArgs a;
     a.x = (const uint16_t*)x;
@@ -327,6 +343,16 @@ ep_status dispatch_impl(const ep_handle* hc, const void* x, ep_quant_mode q, con
     a.H = h->H; a.K = h->K; a.E = tokens ? 1 : h->E; a.nvec = h->H / 8;
     a.row_bytes = (int32_t)db;
     a.scale_bytes = (int32_t)sb;
+    a.scales_t = block_major ? 1 : 0;
+    a.scale_elem = is_mx(q) ? 1 : 4;
+    a.xs = (const uint8_t*)x_scales;
+    a.recv_src = tokens ? h->recv_src_tok : h->recv_src;
+    // block-major MX / per-group scales of the fused path (one encoding per
+    // token) go through the per-token staging rows; per-expert input scales
+    // encode each destination separately and store their scales directly
+    a.src_scales = (block_major && !pre && (is_mx(q) || is_group(q)) && kind != EP_SCALES_PER_EXPERT)
+                       ? h->src_scales : nullptr;
+    if (pre) return from_cuda(launch_dispatch_bytes(h, a, (cudaStream_t)stream));
     return from_cuda(launch_dispatch(h, a, (int)q, (cudaStream_t)stream));
 }
 
@@ -343,6 +369,17 @@ ep_status ep_dispatch_tokens(const ep_handle* hc, const void* x, ep_quant_mode q
                              ep_stream_t stream) {
     if (kind == EP_SCALES_PER_EXPERT) return EP_ERR_UNSUPPORTED;
     return dispatch_impl(hc, x, q, scales, kind, recv_data, recv_scales, cap, stream, true);
+}
+
+ep_status ep_dispatch_ex(const ep_handle* hc, const void* x, const void* x_scales, ep_quant_mode q,
+                         const float* scales, ep_scale_kind kind, uint32_t flags, void* recv_data,
+                         void* recv_scales, int64_t cap, ep_stream_t stream) {
+    const uint32_t known = EP_DISPATCH_PER_RANK | EP_DISPATCH_SCALES_BLOCK_MAJOR | EP_DISPATCH_PRE_ENCODED;
+    if (flags & ~known) return EP_ERR_INVALID_ARG;
+    const bool tokens = (flags & EP_DISPATCH_PER_RANK) != 0;
+    if (tokens && kind == EP_SCALES_PER_EXPERT) return EP_ERR_UNSUPPORTED;
+    return dispatch_impl(hc, x, q, scales, kind, recv_data, recv_scales, cap, stream, tokens, x_scales,
+                         flags);
 }
 
 ep_status ep_token_layout(ep_handle* h, const int64_t* topk, const float* w, const uint8_t* mask,
@@ -387,7 +424,8 @@ ep_status ep_combine_tokens(const ep_handle* hc, const void* y, int64_t y_cap, c
     if (!h) return EP_ERR_INVALID_ARG;
     if (S < 0 || S > kMaxShared || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
     if (y_cap < 0) return EP_ERR_INVALID_ARG;
-    if ((rank_w == nullptr) != (out_w == nullptr)) return EP_ERR_INVALID_ARG;
+    // with no tokens an empty out_weights may come as NULL: nothing to write
+    if (h->N > 0 && (rank_w == nullptr) != (out_w == nullptr)) return EP_ERR_INVALID_ARG;
     if (h->N > 0) {
         if (!out || !aligned_to(out, 16)) return EP_ERR_INVALID_ARG;
         if (y_cap > 0 && (!y || !aligned_to(y, 16))) return EP_ERR_INVALID_ARG;
@@ -405,7 +443,7 @@ ep_status ep_combine_tokens(const ep_handle* hc, const void* y, int64_t y_cap, c
     a.cap = y_cap;
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = 1; a.S = S; a.nvec = h->H / 8;
     cudaError_t err = launch_combine(h, a, (cudaStream_t)stream);
-    if (err == cudaSuccess && rank_w)
+    if (err == cudaSuccess && rank_w && out_w)
         err = launch_reduce_token_weights(h, rank_w, out_w, y_cap, (cudaStream_t)stream);
     return from_cuda(err);
 }

@@ -57,6 +57,9 @@ struct ep_handle {
     int32_t* tok_total;     // [R] tokens received by each rank
     int64_t* tok_base;      // [R+1] first row of each rank
     int32_t* tok_meta;      // [4] {0, rows, rows, 0}: one segment, no padding
+    // per-source-token scale rows of the fused dispatch, staged for the
+    // block-major scale layout: [N][max(H/32, 4)] bytes
+    uint8_t* src_scales;
 };
 
 // Argument block shared by the three layout kernels.
@@ -119,6 +122,18 @@ struct DispatchArgs {
     int64_t cap;
     int32_t H, K, E, nvec;    // nvec = H / 8 (16-byte vectors per bf16 row)
     int32_t row_bytes, scale_bytes;
+    // Block-major receive scales: element b of row r at b * cap + r (units of
+    // scale_elem bytes).  Otherwise row-major [cap][scale_bytes].
+    int32_t scales_t;
+    int32_t scale_elem;       // bytes of one scale element: 1 (e8m0) or 4 (float32)
+    // Pre-encoded source: x points at [N][row_bytes] encoded rows and xs at
+    // [N][scale_bytes] scale rows (null when the mode has none).
+    const uint8_t* xs;
+    const int32_t* recv_src;  // source token of each receive row (-1: padding)
+    // Fused dispatch with block-major MX / per-group scales: each token's scale
+    // row is written once here ([N][scale_bytes]) and a gather pass builds the
+    // block-major columns; null otherwise.
+    uint8_t* src_scales;
 };
 
 struct CombineArgs {
@@ -150,6 +165,8 @@ struct IdentityArgs {
 cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t* mask,
                           int mask_dims, cudaStream_t st);
 cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st);
+// Pre-encoded rows (a.xs / a.x hold encoded bytes): a byte move of data and scale rows.
+cudaError_t launch_dispatch_bytes(const ep_handle* h, const DispatchArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant, cudaStream_t st);
 cudaError_t launch_token_layout(const ep_handle* h, const TokenLayoutArgs& a, cudaStream_t st);

@@ -34,6 +34,8 @@ QUANT_MODES = (EP_QUANT_NONE, EP_QUANT_INT8_STATIC, EP_QUANT_INT8_PER_TOKEN, EP_
                EP_QUANT_FP8_E5M2_PER_TOKEN, EP_QUANT_FP8_E4M3_PER_GROUP, EP_QUANT_FP8_E5M2_PER_GROUP)
 
 EP_SCALES_NONE, EP_SCALES_SCALAR, EP_SCALES_PER_CHANNEL, EP_SCALES_PER_EXPERT = 0, 1, 2, 3
+# ep_dispatch_flag bits of ep_dispatch_ex
+EP_DISPATCH_PER_RANK, EP_DISPATCH_SCALES_BLOCK_MAJOR, EP_DISPATCH_PRE_ENCODED = 1, 2, 4
 
 
 class EPError(RuntimeError):
@@ -95,6 +97,7 @@ def _load():
         "ep_dispatch_tokens": ([vp, vp, st, vp, st, vp, vp, i64, vp], st),
         "ep_combine_tokens": ([vp, vp, i64, vp, i32, vp, vp, vp, vp], st),
         "ep_expert_identity_tokens": ([vp, st, vp, vp, vp, vp, i64, i32, vp, vp], st),
+        "ep_dispatch_ex": ([vp, vp, vp, st, vp, st, ctypes.c_uint32, vp, vp, i64, vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -208,6 +211,13 @@ def ep_dispatch_scaled(h: int, x, quant: int, scales, scale_kind: int, recv_data
     _check(_lib.ep_dispatch_scaled(h, _ptr(x), quant, _ptr(scales), int(scale_kind), _ptr(recv_data),
                                    _ptr(recv_scales), int(recv_rows_capacity), _stream(stream)),
            "ep_dispatch_scaled")
+
+
+def ep_dispatch_ex(h: int, x, x_scales, quant: int, scales, scale_kind: int, flags: int, recv_data,
+                   recv_scales, recv_rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_dispatch_ex(h, _ptr(x), _ptr(x_scales), quant, _ptr(scales), int(scale_kind),
+                               int(flags), _ptr(recv_data), _ptr(recv_scales), int(recv_rows_capacity),
+                               _stream(stream)), "ep_dispatch_ex")
 
 
 def ep_combine(h: int, y, y_rows_capacity: int, topk_weights, shared, num_shared: int, out,
@@ -367,6 +377,28 @@ class EPLayout:
             ep_dispatch(self.h, x, quant, recv_data, recv_scales, cap, stream)
         else:
             ep_dispatch_scaled(self.h, x, quant, scales, scale_kind, recv_data, recv_scales, cap, stream)
+
+    def alloc_recv_block_major(self, quant: int, rows: int, device="cuda"):
+        """Receive buffers whose scales are block-major: (blocks, rows) elements,
+        uint8 [blocks, rows * element bytes]."""
+        db, sb = ep_recv_row_bytes(self.H, quant)
+        es = 1 if quant in (EP_QUANT_MXFP8_E4M3, EP_QUANT_MXFP8_E5M2, EP_QUANT_MXFP4_E2M1) else 4
+        data = torch.empty((rows, db), dtype=torch.uint8, device=device)
+        scales = torch.empty((sb // es, rows * es), dtype=torch.uint8, device=device) if sb else None
+        return data, scales
+
+    def dispatch_ex(self, x: torch.Tensor, quant: int, recv_data: torch.Tensor,
+                    recv_scales: torch.Tensor | None, stream=None, *, x_scales=None, scales=None,
+                    scale_kind: int = EP_SCALES_NONE, per_rank: bool = False,
+                    block_major: bool = False, pre_encoded: bool = False) -> None:
+        """ep_dispatch_ex: pre_encoded moves (x, x_scales) byte rows unchanged;
+        block_major writes the scales (blocks, capacity)."""
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        flags = ((EP_DISPATCH_PER_RANK if per_rank else 0) |
+                 (EP_DISPATCH_SCALES_BLOCK_MAJOR if block_major else 0) |
+                 (EP_DISPATCH_PRE_ENCODED if pre_encoded else 0))
+        ep_dispatch_ex(self.h, x, x_scales, quant, scales, scale_kind, flags, recv_data, recv_scales,
+                       recv_data.numel() // db, stream)
 
     def combine(self, y: torch.Tensor, topk_weights: torch.Tensor, out: torch.Tensor,
                 shared: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -220,3 +220,23 @@ def gen_mask(w: Workload, dims: int, p_active: float = 0.9, stream: int = 8) -> 
     rng = _rng(w, stream)
     shape = (w.R, w.T) if dims == 1 else (w.R, w.T, w.K)
     return (rng.random(shape) < p_active).astype(np.uint8)
+
+
+def gen_encoded_rows(w: Workload, data_bytes: int, scale_bytes: int, stream: int = 9):
+    """Already-encoded source rows for the pre-encoded dispatch: uint8 data
+    [N, data_bytes] and scales [N, scale_bytes], every byte uniform in [0, 256).
+    The dispatch moves these bytes without reading them as numbers, so any
+    byte pattern is a valid input."""
+    rng = _rng(w, stream)
+    data = rng.integers(0, 256, size=(w.N, data_bytes), dtype=np.uint8)
+    scales = rng.integers(0, 256, size=(w.N, scale_bytes), dtype=np.uint8)
+    return data, scales
+
+
+def gen_encoded_rows_device(w: Workload, data_bytes: int, scale_bytes: int, device="cuda"):
+    """gen_encoded_rows drawn on the GPU (torch Philox, seeded) for full sizes."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed + 4099)
+    data = torch.randint(0, 256, (w.N, data_bytes), generator=g, device=device, dtype=torch.uint8)
+    scales = torch.randint(0, 256, (w.N, scale_bytes), generator=g, device=device, dtype=torch.uint8)
+    return data, scales

@@ -339,6 +339,45 @@ ep_status ep_expert_identity_tokens(const ep_handle* handle, ep_quant_mode quant
                                     int64_t rows_capacity, int32_t mark_mod, void* y,
                                     ep_stream_t stream);
 
+/* ---- Alternate input and output formats ---------------------------------- */
+
+/* Flags of ep_dispatch_ex (bitwise or). */
+typedef enum ep_dispatch_flag {
+    /* Target the per-rank layout of ep_token_layout (as ep_dispatch_tokens);
+     * otherwise the per-expert layout of ep_layout. */
+    EP_DISPATCH_PER_RANK = 1,
+    /* Write the receive scales block-major: Modular MAX "EPBatchManager",
+     * ep_dispatch returns, FP8 output_scales of shape (hidden // block_size,
+     * max_recv_tokens).  Scale element b of receive row r goes to element
+     * b * recv_rows_capacity + r of recv_scales, an element being the mode's
+     * scale unit (one e8m0 byte per 32 elements for the MX modes, one float32
+     * per 128-element group, one float32 per row for the per-token modes,
+     * which makes that layout the same as the row-major one).  recv_scales
+     * then holds (scale_bytes / element size) * recv_rows_capacity elements;
+     * padding rows' entries are zero. */
+    EP_DISPATCH_SCALES_BLOCK_MAJOR = 2,
+    /* x (and x_scales) already hold encoded rows: DeepEP "Normal Mode API",
+     * Quantization, x passed as a (data, scale) tuple of MXFP8 / MXFP4 rows.
+     * x is [R*T, data_bytes] and x_scales [R*T, scale_bytes] in the format of
+     * ep_recv_row_bytes(quant); each row's bytes move unchanged (no decode,
+     * no re-encode).  Any quant mode's row format is accepted. */
+    EP_DISPATCH_PRE_ENCODED = 4
+} ep_dispatch_flag;
+
+/* Device.  Dispatch with alternate formats (flags: ep_dispatch_flag).  Without
+ * flags it is ep_dispatch_scaled.  With EP_DISPATCH_PRE_ENCODED, scale_kind
+ * must be EP_SCALES_NONE, x must be 16-byte aligned with data_bytes a multiple
+ * of 16 (else EP_ERR_UNSUPPORTED: the rows move by bulk copies), and
+ * x_scales (4-byte aligned) is required when the mode has scale bytes;
+ * otherwise x_scales must be NULL.  EP_DISPATCH_PER_RANK excludes
+ * EP_SCALES_PER_EXPERT.  Layouts of recv_data, capacity and errors as for
+ * ep_dispatch; recv_scales is row-major [recv_rows_capacity, scale_bytes]
+ * unless EP_DISPATCH_SCALES_BLOCK_MAJOR is set. */
+ep_status ep_dispatch_ex(const ep_handle* handle, const void* x, const void* x_scales,
+                         ep_quant_mode quant, const float* scales, ep_scale_kind scale_kind,
+                         uint32_t flags, void* recv_data, void* recv_scales,
+                         int64_t recv_rows_capacity, ep_stream_t stream);
+
 /* Writable device arrays of one layout, for ep_layout_static_scratch.  Shapes
  * as in ep_layout_views; status is one int32 word (the sticky status word). */
 typedef struct ep_layout_outputs {

@@ -218,3 +218,25 @@ def test_token_layout_validation():
     assert L.ep_combine_tokens(h, A, 10, None, 0, B, C, None, None) == ep.EP_ERR_INVALID_ARG  # weights pair
     assert L.ep_expert_identity_tokens(h, 0, A, None, None, B, 4, 0, C, None) == ep.EP_ERR_INVALID_ARG
     ep.ep_handle_destroy(h)
+
+
+def test_dispatch_ex_validation():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C, D = 1 << 40, 1 << 41, 1 << 42, 1 << 43
+    PRE, BM, RANK = ep.EP_DISPATCH_PRE_ENCODED, ep.EP_DISPATCH_SCALES_BLOCK_MAJOR, ep.EP_DISPATCH_PER_RANK
+    assert L.ep_dispatch_ex(h, A, None, 4, None, 0, 8, B, C, 10, None) == ep.EP_ERR_INVALID_ARG   # unknown flag
+    assert L.ep_dispatch_ex(h, A, None, 4, None, 0, PRE, B, C, 10, None) == ep.EP_ERR_INVALID_ARG  # no x_scales
+    assert L.ep_dispatch_ex(h, A, D + 2, 4, None, 0, PRE, B, C, 10, None) == ep.EP_ERR_INVALID_ARG  # unaligned
+    assert L.ep_dispatch_ex(h, A, D, 0, None, 0, PRE, B, None, 10, None) == ep.EP_ERR_INVALID_ARG  # bf16 has none
+    assert L.ep_dispatch_ex(h, A, D, 2, C, 2, PRE, B, C, 10, None) == ep.EP_ERR_INVALID_ARG  # scales on encoded rows
+    assert L.ep_dispatch_ex(h, A, D, 4, None, 0, BM, B, C, 10, None) == ep.EP_ERR_INVALID_ARG  # x_scales w/o PRE
+    assert L.ep_dispatch_ex(h, A, None, 2, C, 3, RANK, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED  # per-expert
+    assert L.ep_dispatch_ex(h, A, None, 11, None, 0, 0, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED
+    ep.ep_handle_destroy(h)
+    # encoded int8 rows of H = 72 bytes are not whole 16-byte units: no bulk copy
+    p = ep.make_params(2, 8, 72, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    assert L.ep_dispatch_ex(h, A, D, 2, None, 0, PRE, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED
+    ep.ep_handle_destroy(h)
