@@ -240,3 +240,31 @@ def gen_encoded_rows_device(w: Workload, data_bytes: int, scale_bytes: int, devi
     data = torch.randint(0, 256, (w.N, data_bytes), generator=g, device=device, dtype=torch.uint8)
     scales = torch.randint(0, 256, (w.N, scale_bytes), generator=g, device=device, dtype=torch.uint8)
     return data, scales
+
+
+RMS_NORM_EPS = 1e-6
+
+
+def gen_residual(w: Workload, stream: int = 10, chunk: int = 1 << 24) -> np.ndarray:
+    """Residual rows of the combine + AddRmsNorm step, [R, T, H] bf16 bits:
+    float32 N(0,1) rounded once to bf16."""
+    rng = _rng(w, stream)
+    out = np.empty((w.N, w.H), np.uint16)
+    rows = max(1, chunk // w.H)
+    for a in range(0, w.N, rows):
+        b = min(w.N, a + rows)
+        out[a:b] = _to_bf16_bits(rng.standard_normal((b - a, w.H), dtype=np.float32))
+    return out.reshape(w.R, w.T, w.H)
+
+
+def gen_gamma(w: Workload, stream: int = 11) -> np.ndarray:
+    """RMSNorm weight gamma [H] bf16 bits: 1 + 0.1 * N(0,1), rounded to bf16."""
+    rng = _rng(w, stream)
+    return _to_bf16_bits((1.0 + 0.1 * rng.standard_normal(w.H)).astype(np.float32))
+
+
+def gen_residual_device(w: Workload, device="cuda") -> torch.Tensor:
+    """gen_residual's recipe drawn on the GPU (torch Philox, seeded) for full sizes."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed + 6007)
+    return torch.randn((w.N, w.H), generator=g, device=device).to(torch.bfloat16).view(w.R, w.T, w.H)

@@ -109,6 +109,7 @@ def _declare(lib):
     lib.oracle_reduce_token_weights.argtypes = [i64, i32, vp, vp, vp]
     lib.oracle_dispatch_bytes.argtypes = [i32, i32, vp, vp, i64, i64, i64, vp]
     lib.oracle_encode_row.argtypes = [i32, i32, vp, vp, vp]
+    lib.oracle_add_rms_norm_ref64.argtypes = [i64, i32, vp, vp, vp, ctypes.c_double, vp, vp, vp]
     return lib
 
 
@@ -535,3 +536,69 @@ def reduce_token_weights(tl: TokenLayout, rank_w: np.ndarray) -> np.ndarray:
     rw = np.ascontiguousarray(rank_w, dtype=np.float32)
     load().oracle_reduce_token_weights(N, tl.K, _p(np.ascontiguousarray(tl.tok_dst)), _p(rw), _p(out))
     return out
+
+
+# ---------------------------------------------------------------------------
+# combine + residual add + RMSNorm (CANN aclnnMoeDistributeCombineAddRmsNorm)
+# ---------------------------------------------------------------------------
+
+def add_rms_norm_ref64(c: np.ndarray, residual_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float):
+    """(x, rstd, y) in float64: x = c + residual, rstd = 1/sqrt(mean(x^2) + eps),
+    y = x * rstd * gamma, per row of c [N, H] (float64)."""
+    c = np.ascontiguousarray(c, dtype=np.float64)
+    N, H = c.shape
+    r = np.ascontiguousarray(residual_bf16, dtype=np.uint16).reshape(N, H)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16).reshape(H)
+    x = np.zeros((N, H), np.float64)
+    rstd = np.zeros(N, np.float64)
+    y = np.zeros((N, H), np.float64)
+    load().oracle_add_rms_norm_ref64(N, H, _p(c), _p(r), _p(g), float(eps), _p(x), _p(rstd), _p(y))
+    return x, rstd, y
+
+
+def combine_add_rms_norm_ref64(lay: Layout, y_bf16: np.ndarray, w: np.ndarray, shared, residual_bf16,
+                               gamma_bf16, eps: float, tok_begin: int = 0, tok_end: int | None = None,
+                               y_rows: np.ndarray | None = None):
+    """Reference of the fused combine + AddRmsNorm for tokens [tok_begin, tok_end):
+    dict with the exact combine sums c and their magnitudes mag, and x, rstd, y."""
+    c, mag = combine_ref64(lay, y_bf16, w, shared, tok_begin, tok_end, y_rows)
+    H = c.shape[1]
+    r = np.ascontiguousarray(residual_bf16, dtype=np.uint16).reshape(-1, H)
+    if r.shape[0] != c.shape[0]:
+        r = r[tok_begin:tok_begin + c.shape[0]]
+    x, rstd, yv = add_rms_norm_ref64(c, r, gamma_bf16, eps)
+    return dict(c=c, mag=mag, x=x, rstd=rstd, y=yv, gamma=bf16_bits_to_f64(gamma_bf16).reshape(H))
+
+
+def add_rms_norm_within_tolerance(x_bits, rstd, y_bits, ref: dict, K: int, S: int):
+    """Derived error bound of a binary32 implementation that rounds the combine
+    to bf16 (|c_bf16 - c| <= t = 2 ulp_bf16(c) + (2K+S+1) 2^-24 mag, as for the
+    combine), adds the residual in binary32, and normalises in binary32:
+      x error   e_i  = t_i + 2^-24 (|x_i| + t_i)
+      sum of squares relative error  s = 2 |e|/|x| + (|e|/|x|)^2 + (H+4) 2^-24
+      rstd relative error  rho = s / (2 (1 - s)) + 3 * 2^-24
+      y error   d_i = |gamma_i| rstd (e_i (1 + rho) + |x_i| rho), plus the
+                two binary32 products (2^-22 |y_i|) and the bf16 rounding
+                (ulp_bf16 of |y_i| + d_i, twice the half-ulp).
+    x_out is checked against e_i + ulp_bf16(|x_i| + e_i).  Returns (ok, worst
+    ratio of error to bound over x, rstd, y)."""
+    c, mag, x, r, y, g = ref["c"], ref["mag"], ref["x"], ref["rstd"], ref["y"], ref["gamma"]
+    H = c.shape[1]
+    t = 2.0 * ulp_bf16(c) + (2 * K + S + 1) * 2.0 ** -24 * mag
+    e = t + 2.0 ** -24 * (np.abs(x) + t)
+    en = np.sqrt((e * e).sum(axis=1))
+    xn = np.sqrt((x * x).sum(axis=1))
+    q = en / np.maximum(xn, 1e-300)
+    s = 2.0 * q + q * q + (H + 4) * 2.0 ** -24
+    assert np.all(s < 0.5), "x too small for a meaningful bound"
+    rho = s / (2.0 * (1.0 - s)) + 3 * 2.0 ** -24
+    out = {}
+    gx = bf16_bits_to_f64(np.asarray(x_bits).reshape(x.shape))
+    bx = e + ulp_bf16(np.abs(x) + e)
+    out["x"] = float(np.max(np.abs(gx - x) / bx)) if x.size else 0.0
+    out["rstd"] = float(np.max(np.abs(np.asarray(rstd, np.float64) - r) / (r * rho))) if r.size else 0.0
+    d = np.abs(g)[None, :] * r[:, None] * (e * (1.0 + rho[:, None]) + np.abs(x) * rho[:, None])
+    by = d * (1.0 + 2.0 ** -20) + 2.0 ** -22 * np.abs(y) + ulp_bf16(np.abs(y) + d)
+    gy = bf16_bits_to_f64(np.asarray(y_bits).reshape(y.shape))
+    out["y"] = float(np.max(np.abs(gy - y) / by)) if y.size else 0.0
+    return all(v <= 1.0 for v in out.values()), out

@@ -748,7 +748,7 @@ void oracle_combine(int R, int T, int H, int K, int S, const int32_t* dst_row,
 }
 
 /* The same sum in binary64, with the sum of the terms' magnitudes, for the
- * combine tolerance (|gpu - ref| <= 2 ulp_bf16(ref) + 2^-20 * sum|terms|). */
+ * combine tolerance (|gpu - ref| <= 2 ulp_bf16(ref) + (2K+S+1) 2^-24 sum|terms|). */
 void oracle_combine_ref64(int R, int T, int H, int K, int S, const int32_t* dst_row,
                           const float* w, const uint16_t* y, const int64_t* y_rows,
                           const uint16_t* shared, int64_t tok_begin, int64_t tok_end,
@@ -774,5 +774,33 @@ void oracle_combine_ref64(int R, int T, int H, int K, int S, const int32_t* dst_
             ref[(n - tok_begin) * H + h] = acc;
             absum[(n - tok_begin) * H + h] = mag;
         }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Combine fused with a residual add and RMSNorm: CANN's                    */
+/* aclnnMoeDistributeCombineAddRmsNorm, which the aclnnMoeDistributeDispatchV2 */
+/* page names as a combine to pair with the dispatch; its formula is not     */
+/* printed there.  Reading taken (the standard AddRmsNorm applied to the     */
+/* combine's output):                                                        */
+/*   x    = combine(row) + residual                                          */
+/*   rstd = 1 / sqrt(mean over the H elements of x^2 + eps)                  */
+/*   y    = x * rstd * gamma                                                 */
+/* In binary64 from binary64 combine values c[N][H] (the exact weighted sums */
+/* of oracle_combine_ref64), bf16 residual[N][H] and gamma[H].               */
+/* ------------------------------------------------------------------------ */
+void oracle_add_rms_norm_ref64(int64_t N, int H, const double* c, const uint16_t* residual,
+                               const uint16_t* gamma, double eps, double* x, double* rstd, double* y) {
+    for (int64_t n = 0; n < N; ++n) {
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double v = c[n * H + h] + (double)oracle_bf16_to_f32(residual[n * H + h]);
+            x[n * H + h] = v;
+            ss += v * v;
+        }
+        double r = 1.0 / sqrt(ss / (double)H + eps);
+        rstd[n] = r;
+        for (int h = 0; h < H; ++h)
+            y[n * H + h] = x[n * H + h] * r * (double)oracle_bf16_to_f32(gamma[h]);
     }
 }

@@ -15,6 +15,7 @@ import pytest
 import oracle
 import test_oracle_dispatch_combine as tdc
 import test_oracle_formats as tfm
+import test_oracle_rms_norm as trn
 import test_oracle_layout as tl
 import test_oracle_quant as tq
 import test_oracle_quant_ext as tqx
@@ -69,6 +70,14 @@ MUTANTS = {
         "memcpy(out + (d - row_begin) * row_bytes, src + d * row_bytes, (size_t)row_bytes);"),
     "bytes_first_slot_only": ("        for (int k = 0; k < K; ++k) {\n            int64_t d = dst_row[n * K + k];\n            if (d < row_begin || d >= row_end) continue;\n            memcpy(out + (d - row_begin) * row_bytes, src + n",
                               "        for (int k = 0; k < 1; ++k) {\n            int64_t d = dst_row[n * K + k];\n            if (d < row_begin || d >= row_end) continue;\n            memcpy(out + (d - row_begin) * row_bytes, src + n"),
+    "rms_residual_dropped": ("double v = c[n * H + h] + (double)oracle_bf16_to_f32(residual[n * H + h]);",
+                             "double v = c[n * H + h];"),
+    "rms_eps_outside_sqrt": ("double r = 1.0 / sqrt(ss / (double)H + eps);",
+                             "double r = 1.0 / (sqrt(ss / (double)H) + eps);"),
+    "rms_mean_over_h_minus_one": ("double r = 1.0 / sqrt(ss / (double)H + eps);",
+                                  "double r = 1.0 / sqrt(ss / (double)(H - 1) + eps);"),
+    "rms_gamma_shifted": ("x[n * H + h] * r * (double)oracle_bf16_to_f32(gamma[h]);",
+                          "x[n * H + h] * r * (double)oracle_bf16_to_f32(gamma[(h + 1) % H]);"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -101,6 +110,8 @@ def pins():
     cases += [lambda: ttl.test_combine_through_rank_expert_stage_closed_form(2, 24, 4),
               ttl.test_reduced_weights_equal_original_for_valid_entries]
     cases += [lambda s=s: tfm.test_dispatch_bytes_brute_force(s) for s in range(4)]
+    cases += [trn.test_hand_worked_row, lambda: trn.test_constant_row(1e-3, 1e-6),
+              lambda: trn.test_constant_row(0.75, 1e-6), lambda: trn.test_matches_torch_rms_norm_float64(1e-6)]
     return cases
 
 
