@@ -54,16 +54,19 @@ WORKLOAD_KEYS = {"1": (1, 0, 0, 0, "expert", ""), "2": (2, 0, 0, 0, "expert", ""
                  # the DeepEP per-rank receive layout
                  "2r": (2, 0, 0, 0, "rank", ""), "4r": (4, 4, 0, 0, "rank", ""),
                  # alternate formats
-                 "4p": (4, 4, 0, 0, "expert", "pre"), "4x": (4, 4, 0, 0, "expert", "bm")}
+                 "4p": (4, 4, 0, 0, "expert", "pre"), "4x": (4, 4, 0, 0, "expert", "bm"),
+                 # combine fused with the residual add and RMSNorm
+                 "2n": (2, 0, 0, 0, "expert", "norm")}
 FORMAT = {"": "bf16 input, row-major scales",
           "pre": "pre-encoded (data, scale) rows moved unchanged",
-          "bm": "block-major scales (blocks, capacity)"}
+          "bm": "block-major scales (blocks, capacity)",
+          "norm": "combine + residual add + RMSNorm (outputs y, x = combine + residual, rstd)"}
 QNAME = {0: "none", 1: "int8_static", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2",
          6: "mxfp4_e2m1", 7: "fp8_e4m3_per_token", 8: "fp8_e5m2_per_token",
          9: "fp8_e4m3_per_group128", 10: "fp8_e5m2_per_group128"}
 SCALE_KIND = {0: "none", 1: "scalar", 2: "per_channel", 3: "per_expert"}
 SAMPLE_NOTE = " (input scales and xActiveMask are not applied in the oracle sample)"
-FORMAT_NOTE = " (the oracle sample runs the fused bf16-input, row-major path of the same mode)"
+FORMAT_NOTE = " (the oracle sample runs the plain path of the same mode, without the format variant)"
 KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "layout": "layout.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
@@ -228,13 +231,14 @@ def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt=""):
     disp = N * H * 2 + N * K * 4 + rows * (db + sb)
     if fmt == "pre":
         disp = N * (db + sb) + N * K * 4 + rows * (db + sb) + (rows * 4 if sb else 0)
+    norm = N * H * 2 * 3 + H * 2 + N * 4 if fmt == "norm" else 0   # residual in; x, rstd out
     lay = N * K * 8 * 3 + N * K * 4 + rows * 4 + N * w.R
     if per_rank:
         comb = rows * H * 2 + N * K * 4 + S * N * H * 2 + N * H * 2
         lay += N * K * (8 + 4 + 4) + rows * (4 + K * 12)
     else:
         comb = V * H * 2 + N * K * 8 + S * N * H * 2 + N * H * 2
-    return {"layout": lay, "dispatch": disp, "combine": comb}
+    return {"layout": lay, "dispatch": disp, "combine": comb + norm}
 
 
 def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_layout="expert",
@@ -276,8 +280,17 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         if per_rank:
             lay.token_layout(topk_t, w_t, active_mask=mask_dev, stream=s, out=(ridx, rw))
 
+    norm = fmt == "norm"
+    if norm:
+        res_dev = synth.gen_residual_device(w, device=dev).view(w.N, w.H)
+        gamma_dev = torch.from_numpy(synth.gen_gamma(w).view(np.int16)).to(dev).view(torch.bfloat16)
+        x_out_dev = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
+        rstd_dev = torch.empty(w.N, dtype=torch.float32, device=dev)
+    else:
+        res_dev = None
+
     def do_dispatch(x_t, s=None, xs_t=None):
-        if fmt:
+        if fmt in ("pre", "bm"):
             lay.dispatch_ex(x_t, quant, data, scales, s, x_scales=xs_t, per_rank=per_rank,
                             pre_encoded=fmt == "pre", block_major=fmt == "bm")
         elif per_rank:
@@ -285,13 +298,16 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         else:
             lay.dispatch(x_t, quant, data, scales, s, scales=sc_dev, scale_kind=kind)
 
-    def do_combine(w_t, out_t, sh_t, s=None):
-        if per_rank:
+    def do_combine(w_t, out_t, sh_t, s=None, res_t=None):
+        if norm:
+            lay.combine_add_rms_norm(y, w_t, res_t if res_t is not None else res_dev, gamma_dev, out_t,
+                                     x_out_dev, rstd_dev, sh_t, synth.RMS_NORM_EPS, s)
+        elif per_rank:
             lay.combine_tokens(y, out_t, sh_t, stream=s)
         else:
             lay.combine(y, w_t, out_t, sh_t, s)
 
-    if quant == 0 and not fmt:
+    if quant == 0 and fmt in ("", "norm"):
         y = data.view(torch.bfloat16).view(-1, w.H)
     elif fmt:
         # expert outputs from the fused row-major path of the same bf16 x
@@ -361,19 +377,22 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
             return h
         x_host = pinned_like(x_dev)
         xs_host = None if xs_dev is None else pinned_like(xs_dev)
+        res_host = None if res_dev is None else pinned_like(res_dev)
         topk_host = torch.from_numpy(topk).pin_memory()
         w_host = torch.from_numpy(wts).pin_memory()
         sh_host = None if sh_dev is None else pinned_like(sh_dev)
         out_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-        slots = [dict(x=x_dev, xs=xs_dev, topk=topk_dev, w=w_dev, sh=sh_dev, out=out)]
+        slots = [dict(x=x_dev, xs=xs_dev, res=res_dev, topk=topk_dev, w=w_dev, sh=sh_dev, out=out)]
         slots.append(dict(x=torch.empty_like(x_dev),
                           xs=None if xs_dev is None else torch.empty_like(xs_dev),
+                          res=None if res_dev is None else torch.empty_like(res_dev),
                           topk=torch.empty_like(topk_dev),
                           w=torch.empty_like(w_dev),
                           sh=None if sh_dev is None else torch.empty_like(sh_dev),
                           out=torch.empty_like(out)))
         h2d = x_host.numel() * x_host.element_size() + topk_host.numel() * 8 + w_host.numel() * 4
         h2d += 0 if xs_host is None else xs_host.numel()
+        h2d += 0 if res_host is None else res_host.numel() * 2
         h2d += 0 if sh_host is None else sh_host.numel() * 2
         d2h = out.numel() * 2
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -391,6 +410,8 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
                     sl["x"].copy_(x_host, non_blocking=True)
                     if xs_host is not None:
                         sl["xs"].copy_(xs_host, non_blocking=True)
+                    if res_host is not None:
+                        sl["res"].copy_(res_host, non_blocking=True)
                     sl["topk"].copy_(topk_host, non_blocking=True)
                     sl["w"].copy_(w_host, non_blocking=True)
                     if sh_host is not None:
@@ -401,7 +422,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
                     s_k.wait_event(ev_out[i - 2])         # slot's output already read back
                 do_layout(sl["topk"], sl["w"], s_k)
                 do_dispatch(sl["x"], s_k, sl["xs"])
-                do_combine(sl["w"], sl["out"], sl["sh"], s_k)
+                do_combine(sl["w"], sl["out"], sl["sh"], s_k, sl["res"])
                 ev_k[i].record(s_k)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_k[i])
@@ -424,7 +445,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         e2e_ms = s2.elapsed_time(t2) / k2
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h, "steps": k2}
         assert lay.status() == ep.EP_OK
-        if quant == 0 and not fmt:
+        if quant == 0 and fmt in ("", "norm"):
             # the copied-back output of the last step equals the device-resident result
             assert torch.equal(out_host[(k2 - 1) % 2].to(dev), out)
 

@@ -32,6 +32,17 @@ __device__ __forceinline__ void acc_fma(float acc[8], const uint4& v, float w) {
     acc[7] = fmaf(w, __uint_as_float(v.w & 0xffff0000u), acc[7]);
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
+
+// x[i] = bf16 element i of c + bf16 element i of r, rounded once to float32.
+__device__ __forceinline__ void acc_add_rn(float x[8], const uint4& c, const uint4& r) {
+    x[0] = __fadd_rn(bf16_lo(c.x), bf16_lo(r.x)); x[1] = __fadd_rn(bf16_hi(c.x), bf16_hi(r.x));
+    x[2] = __fadd_rn(bf16_lo(c.y), bf16_lo(r.y)); x[3] = __fadd_rn(bf16_hi(c.y), bf16_hi(r.y));
+    x[4] = __fadd_rn(bf16_lo(c.z), bf16_lo(r.z)); x[5] = __fadd_rn(bf16_hi(c.z), bf16_hi(r.z));
+    x[6] = __fadd_rn(bf16_lo(c.w), bf16_lo(r.w)); x[7] = __fadd_rn(bf16_hi(c.w), bf16_hi(r.w));
+}
+
 __device__ __forceinline__ void acc_add(float acc[8], const uint4& v) {
     acc[0] += __uint_as_float(v.x << 16);
     acc[1] += __uint_as_float(v.x & 0xffff0000u);
@@ -71,6 +82,15 @@ constexpr int kMetaInts = 32;   // per stage: [0] = valid slots, [1..16] = weigh
 #define EP_COMBINE_MAX_THREADS 512
 #endif
 
+// NORM: the residual add + RMSNorm epilogue (CANN
+// aclnnMoeDistributeCombineAddRmsNorm).  The producer also loads the chunk of
+// the token's residual row into the stage; consumers round the combine to
+// bf16, add the residual in float32, write bf16(x), keep x in a shared-memory
+// row buffer (each thread reads back only what it wrote) and accumulate x^2.
+// After the row's last chunk the consumer warps reduce the sum of squares
+// through a per-token-parity slot array and mbarrier (bounded waits), then
+// write y = x * rstd * gamma for the whole row and rstd.
+template <bool NORM>
 __global__ void __launch_bounds__(32 + EP_COMBINE_MAX_THREADS)
 combine_tma_kernel(CombineArgs a, CombineTma c) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -78,6 +98,10 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
     int32_t* meta = reinterpret_cast<int32_t*>(smem + (size_t)c.nstages * c.stage_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(meta + c.nstages * kMetaInts);
     uint64_t* empty = full + c.nstages;
+    uint64_t* redbar = empty + c.nstages;                         // NORM: [2]
+    float* red = reinterpret_cast<float*>(redbar + 2);            // NORM: [2][32]
+    float* xbuf = red + 64;                                       // NORM: [H]
+    uint16_t* gbuf = reinterpret_cast<uint16_t*>(xbuf + a.H);     // NORM: gamma [H]
     const int total = a.expert_base[a.E];
     if ((int64_t)total > a.cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
@@ -90,7 +114,16 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], ncw);
         }
+        if (NORM) {
+            mbar_init(&redbar[0], ncw);
+            mbar_init(&redbar[1], ncw);
+        }
         mbar_fence_init();
+    }
+    if constexpr (NORM) {
+        // gamma is read once per token row: keep it in shared memory
+        for (int v = tid; v < a.nvec; v += blockDim.x)
+            reinterpret_cast<uint4*>(gbuf)[v] = ld_nc_v4(a.gamma + v * 8);
     }
     __syncthreads();
     const int64_t G = gridDim.x;
@@ -137,7 +170,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
                 }
                 if (lane == 0) {
                     m[0] = kv;
-                    mbar_arrive_expect_tx(&full[s], cb * (uint32_t)(kv + a.S));
+                    mbar_arrive_expect_tx(&full[s], cb * (uint32_t)(kv + a.S + (NORM ? 1 : 0)));
                 }
                 __syncwarp();
                 uint8_t* st = stages + (size_t)s * c.stage_bytes;
@@ -145,6 +178,8 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
                 if (lane < a.S)
                     bulk_load(st + (size_t)(kv + lane) * rowb,
                               a.shared + ((sr * a.S + lane) * a.T + tt) * a.H + e0, cb, &full[s]);
+                if (NORM && lane == a.S)
+                    bulk_load(st + (size_t)(kv + a.S) * rowb, a.residual + n * a.H + e0, cb, &full[s]);
             }
         }
         if (!ok && lane == 0) ep_set_status(a.status, EP_ERR_TIMEOUT);
@@ -157,6 +192,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
     const int ct = (tid - 32) - g * c.nconsumer;
     const int64_t items = cnt * c.nch;
     bool ok = true;
+    float ss = 0.0f;   // NORM: this thread's part of the row's sum of x^2
     for (int64_t q = g; q < items; q += c.ngroups) {
         const int64_t j = q / c.nch;
         const int ci = (int)(q - j * c.nch);
@@ -183,10 +219,67 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
             o.y = pack_bf16x2_rn(acc[2], acc[3]);
             o.z = pack_bf16x2_rn(acc[4], acc[5]);
             o.w = pack_bf16x2_rn(acc[6], acc[7]);
-            st_v4(a.out + n * a.H + e0 + v * 8, o);
+            if constexpr (NORM) {
+                // x = bf16(combine) + residual, in float32
+                float x[8];
+                acc_add_rn(x, o, lds_v4(col + (size_t)(kv + a.S) * rowb));
+                float4* xb = reinterpret_cast<float4*>(xbuf + e0 + v * 8);
+                xb[0] = make_float4(x[0], x[1], x[2], x[3]);
+                xb[1] = make_float4(x[4], x[5], x[6], x[7]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+                if (a.x_out) {
+                    uint4 xo;
+                    xo.x = pack_bf16x2_rn(x[0], x[1]);
+                    xo.y = pack_bf16x2_rn(x[2], x[3]);
+                    xo.z = pack_bf16x2_rn(x[4], x[5]);
+                    xo.w = pack_bf16x2_rn(x[6], x[7]);
+                    st_v4(a.x_out + n * a.H + e0 + v * 8, xo);
+                }
+            } else {
+                st_v4(a.out + n * a.H + e0 + v * 8, o);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if constexpr (NORM) {
+            if (ci == c.nch - 1) {
+                // the row is complete: reduce the sum of squares over the consumer warps
+                float t = ss;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+                const int par = (int)(j & 1);
+                if (lane == 0) {
+                    red[par * 32 + ((tid - 32) >> 5)] = t;
+                    mbar_arrive(&redbar[par]);
+                }
+                if (!mbar_wait(&redbar[par], (uint32_t)((j >> 1) & 1), kMaxPolls)) { ok = false; break; }
+                float sum = 0.0f;
+                for (int wi = 0; wi < ncw; ++wi) sum += red[par * 32 + wi];
+                const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, (float)a.H), a.eps)));
+                if (ct == 0 && a.rstd) a.rstd[n] = rs;
+                for (int c2 = 0; c2 < c.nch; ++c2) {
+                    const int f0 = c2 * c.CH;
+                    const int nv2 = min(c.CH, a.H - f0) >> 3;
+                    for (int v = ct; v < nv2; v += c.nconsumer) {
+                        const float4* xb = reinterpret_cast<const float4*>(xbuf + f0 + v * 8);
+                        const float4 x0 = xb[0], x1 = xb[1];
+                        const uint4 gv = lds_v4(gbuf + f0 + v * 8);
+                        uint4 yo;
+                        yo.x = pack_bf16x2_rn(__fmul_rn(__fmul_rn(x0.x, rs), bf16_lo(gv.x)),
+                                              __fmul_rn(__fmul_rn(x0.y, rs), bf16_hi(gv.x)));
+                        yo.y = pack_bf16x2_rn(__fmul_rn(__fmul_rn(x0.z, rs), bf16_lo(gv.y)),
+                                              __fmul_rn(__fmul_rn(x0.w, rs), bf16_hi(gv.y)));
+                        yo.z = pack_bf16x2_rn(__fmul_rn(__fmul_rn(x1.x, rs), bf16_lo(gv.z)),
+                                              __fmul_rn(__fmul_rn(x1.y, rs), bf16_hi(gv.z)));
+                        yo.w = pack_bf16x2_rn(__fmul_rn(__fmul_rn(x1.z, rs), bf16_lo(gv.w)),
+                                              __fmul_rn(__fmul_rn(x1.w, rs), bf16_hi(gv.w)));
+                        st_v4(a.out + n * a.H + f0 + v * 8, yo);
+                    }
+                }
+                ss = 0.0f;
+            }
+        }
     }
     if (!ok && lane == 0) ep_set_status(a.status, EP_ERR_TIMEOUT);
 }
@@ -336,13 +429,22 @@ identity_tokens_kernel(IdentityArgs a, const int64_t* ridx, const float* rw, int
 
 }  // namespace
 
-cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st) {
+namespace {
+
+template <bool NORM>
+cudaError_t launch_combine_impl(const ep_handle* h, const CombineArgs& a, cudaStream_t st) {
     if (a.N == 0) return cudaSuccess;
     CombineTma c;
-    c.rows = a.K + a.S;
-    // about EP_COMBINE_STAGE_TARGET bytes of row chunks per stage, chunks of
-    // equal size (multiples of 8 elements)
-    int ch = (EP_COMBINE_STAGE_TARGET / 2 / c.rows) & ~7;
+    c.rows = a.K + a.S + (NORM ? 1 : 0);
+    // NORM: two reduction barriers, two 32-slot partial-sum arrays, the x row
+    // (float32) and gamma (bf16)
+    const int norm_bytes = NORM ? 16 + 2 * 32 * 4 + a.H * 4 + a.H * 2 : 0;
+    // about EP_COMBINE_STAGE_TARGET bytes of row chunks per stage (with the x
+    // row buffer, small enough for three stages), chunks of equal size
+    // (multiples of 8 elements)
+    int target = EP_COMBINE_STAGE_TARGET;
+    if (NORM && target > (kCombineSmemBudget - norm_bytes) / 3) target = (kCombineSmemBudget - norm_bytes) / 3;
+    int ch = (target / 2 / c.rows) & ~7;
     if (ch < 8) ch = 8;
     if (ch > a.H) ch = a.H;
     int nch = (a.H + ch - 1) / ch;
@@ -352,12 +454,15 @@ cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_
     c.nch = nch;
     c.stage_bytes = (c.rows * ch * 2 + 127) / 128 * 128;
     const int per_stage = c.stage_bytes + kMetaInts * 4 + 16;
-    c.nstages = kCombineSmemBudget / per_stage;
+    c.nstages = (kCombineSmemBudget - norm_bytes) / per_stage;
     if (c.nstages > 16) c.nstages = 16;
     if (c.nstages < 2) return cudaErrorInvalidConfiguration;
     c.nconsumer = ((ch / 8 + 31) / 32) * 32;
-    if (c.nconsumer > 256) c.nconsumer = 256;
-    c.ngroups = EP_COMBINE_GROUPS;
+    // NORM keeps one group: let it cover a whole chunk in one pass
+    const int max_consumer = NORM ? EP_COMBINE_MAX_THREADS : 256;
+    if (c.nconsumer > max_consumer) c.nconsumer = max_consumer;
+    // the epilogue reduces a whole row inside one consumer group
+    c.ngroups = NORM ? 1 : EP_COMBINE_GROUPS;
     while (c.ngroups > 1 && c.ngroups * c.nconsumer > EP_COMBINE_MAX_THREADS) --c.ngroups;
     if (c.ngroups > c.nstages) c.ngroups = c.nstages;
     if (c.ngroups < 1) c.ngroups = 1;
@@ -366,14 +471,26 @@ cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_
     // group then waits on a stage's uses in order and is never more than one
     // phase ahead of its "full" barrier (phase-parity waits cannot alias).
     c.nstages = c.nstages / c.ngroups * c.ngroups;
-    const size_t smem = (size_t)c.nstages * per_stage;
-    cudaError_t err = cudaFuncSetAttribute(combine_tma_kernel,
+    // 8-byte alignment of the barriers after the per-stage metadata: stage_bytes
+    // is a multiple of 128 and kMetaInts * 4 of 8
+    const size_t smem = (size_t)c.nstages * per_stage + norm_bytes;
+    cudaError_t err = cudaFuncSetAttribute(combine_tma_kernel<NORM>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     int64_t grid = h->num_sms;
     if (grid > a.N) grid = a.N;
-    combine_tma_kernel<<<(unsigned)grid, 32 + c.ngroups * c.nconsumer, smem, st>>>(a, c);
+    combine_tma_kernel<NORM><<<(unsigned)grid, 32 + c.ngroups * c.nconsumer, smem, st>>>(a, c);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st) {
+    return launch_combine_impl<false>(h, a, st);
+}
+
+cudaError_t launch_combine_norm(const ep_handle* h, const CombineArgs& a, cudaStream_t st) {
+    return launch_combine_impl<true>(h, a, st);
 }
 
 cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant, cudaStream_t st) {

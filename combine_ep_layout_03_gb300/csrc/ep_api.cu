@@ -442,6 +442,7 @@ ep_status ep_combine_tokens(const ep_handle* hc, const void* y, int64_t y_cap, c
     a.N = h->N;
     a.cap = y_cap;
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = 1; a.S = S; a.nvec = h->H / 8;
+    a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
     cudaError_t err = launch_combine(h, a, (cudaStream_t)stream);
     if (err == cudaSuccess && rank_w && out_w)
         err = launch_reduce_token_weights(h, rank_w, out_w, y_cap, (cudaStream_t)stream);
@@ -499,7 +500,44 @@ ep_status ep_combine(const ep_handle* hc, const void* y, int64_t y_cap, const fl
     a.N = h->N;
     a.cap = y_cap;
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
+    a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
     return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
+}
+
+ep_status ep_combine_add_rms_norm(const ep_handle* hc, const void* y, int64_t y_cap, const float* w,
+                                  const void* shared, int32_t S, const void* residual, const void* gamma,
+                                  float eps, void* norm_out, void* x_out, float* rstd_out,
+                                  ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (S < 0 || S > kMaxShared || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
+    if (y_cap < 0) return EP_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return EP_ERR_INVALID_ARG;   // also rejects NaN
+    if (h->N > 0) {
+        if (!w || !aligned_to(w, 4) || !norm_out || !aligned_to(norm_out, 16)) return EP_ERR_INVALID_ARG;
+        if (!residual || !aligned_to(residual, 16) || !gamma || !aligned_to(gamma, 16)) return EP_ERR_INVALID_ARG;
+        if (x_out && !aligned_to(x_out, 16)) return EP_ERR_INVALID_ARG;
+        if (rstd_out && !aligned_to(rstd_out, 4)) return EP_ERR_INVALID_ARG;
+        if (y_cap > 0 && (!y || !aligned_to(y, 16))) return EP_ERR_INVALID_ARG;
+    }
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    CombineArgs a;
+    a.y = (const uint16_t*)y;
+    a.w = w;
+    a.shared = (const uint16_t*)shared;
+    a.out = (uint16_t*)norm_out;
+    a.dst_row = h->dst_row;
+    a.expert_base = h->expert_base;
+    a.status = h->status;
+    a.N = h->N;
+    a.cap = y_cap;
+    a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
+    a.residual = (const uint16_t*)residual;
+    a.gamma = (const uint16_t*)gamma;
+    a.eps = eps;
+    a.x_out = (uint16_t*)x_out;
+    a.rstd = rstd_out;
+    return from_cuda(launch_combine_norm(h, a, (cudaStream_t)stream));
 }
 
 ep_status ep_expert_identity(const ep_handle* hc, ep_quant_mode q, const void* recv_data,

@@ -147,6 +147,13 @@ struct CombineArgs {
     int64_t N;
     int64_t cap;
     int32_t T, H, K, E, S, nvec;
+    // Residual add + RMSNorm epilogue (launch_combine_norm only): out receives
+    // y = x * rstd * gamma with x = bf16(combine) + residual in float32.
+    const uint16_t* residual; // [N][H] bf16
+    const uint16_t* gamma;    // [H] bf16
+    float eps;
+    uint16_t* x_out;          // [N][H] bf16(x), or null
+    float* rstd;              // [N], or null
 };
 
 struct IdentityArgs {
@@ -168,6 +175,8 @@ cudaError_t launch_dispatch(const ep_handle* h, const DispatchArgs& a, int quant
 // Pre-encoded rows (a.xs / a.x hold encoded bytes): a byte move of data and scale rows.
 cudaError_t launch_dispatch_bytes(const ep_handle* h, const DispatchArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const ep_handle* h, const CombineArgs& a, cudaStream_t st);
+// Combine followed by the residual add and RMSNorm (a.residual, a.gamma set).
+cudaError_t launch_combine_norm(const ep_handle* h, const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant, cudaStream_t st);
 cudaError_t launch_token_layout(const ep_handle* h, const TokenLayoutArgs& a, cudaStream_t st);
 cudaError_t launch_reduce_token_weights(const ep_handle* h, const float* rank_w, float* out_w,

@@ -98,6 +98,7 @@ def _load():
         "ep_combine_tokens": ([vp, vp, i64, vp, i32, vp, vp, vp, vp], st),
         "ep_expert_identity_tokens": ([vp, st, vp, vp, vp, vp, i64, i32, vp, vp], st),
         "ep_dispatch_ex": ([vp, vp, vp, st, vp, st, ctypes.c_uint32, vp, vp, i64, vp], st),
+        "ep_combine_add_rms_norm": ([vp, vp, i64, vp, vp, i32, vp, vp, ctypes.c_float, vp, vp, vp, vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -218,6 +219,14 @@ def ep_dispatch_ex(h: int, x, x_scales, quant: int, scales, scale_kind: int, fla
     _check(_lib.ep_dispatch_ex(h, _ptr(x), _ptr(x_scales), quant, _ptr(scales), int(scale_kind),
                                int(flags), _ptr(recv_data), _ptr(recv_scales), int(recv_rows_capacity),
                                _stream(stream)), "ep_dispatch_ex")
+
+
+def ep_combine_add_rms_norm(h: int, y, y_rows_capacity: int, topk_weights, shared, num_shared: int,
+                            residual, gamma, eps: float, norm_out, x_out, rstd_out, stream=None) -> None:
+    _check(_lib.ep_combine_add_rms_norm(h, _ptr(y), int(y_rows_capacity), _ptr(topk_weights), _ptr(shared),
+                                        int(num_shared), _ptr(residual), _ptr(gamma), float(eps),
+                                        _ptr(norm_out), _ptr(x_out), _ptr(rstd_out), _stream(stream)),
+           "ep_combine_add_rms_norm")
 
 
 def ep_combine(h: int, y, y_rows_capacity: int, topk_weights, shared, num_shared: int, out,
@@ -406,6 +415,16 @@ class EPLayout:
         cap = y.numel() // self.H
         ep_combine(self.h, y, cap, topk_weights, shared, S, out, stream)
         return out
+
+    def combine_add_rms_norm(self, y: torch.Tensor, topk_weights: torch.Tensor, residual: torch.Tensor,
+                             gamma: torch.Tensor, norm_out: torch.Tensor, x_out: torch.Tensor | None = None,
+                             rstd_out: torch.Tensor | None = None, shared: torch.Tensor | None = None,
+                             eps: float = 1e-6, stream=None) -> torch.Tensor:
+        """Combine, then x = combine + residual and norm_out = RMSNorm(x) * gamma."""
+        S = 0 if shared is None else shared.shape[1]
+        ep_combine_add_rms_norm(self.h, y, y.numel() // self.H, topk_weights, shared, S, residual, gamma,
+                                eps, norm_out, x_out, rstd_out, stream)
+        return norm_out
 
     def expert_identity(self, quant: int, recv_data, recv_scales, y, mark_mod: int = 0,
                         stream=None) -> torch.Tensor:

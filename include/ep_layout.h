@@ -378,6 +378,26 @@ ep_status ep_dispatch_ex(const ep_handle* handle, const void* x, const void* x_s
                          uint32_t flags, void* recv_data, void* recv_scales,
                          int64_t recv_rows_capacity, ep_stream_t stream);
 
+/* ---- Combine with residual add and RMSNorm -------------------------------- */
+
+/* Device.  CANN's aclnnMoeDistributeCombineAddRmsNorm (named on the
+ * aclnnMoeDistributeDispatchV2 page as a combine that pairs with the
+ * dispatch; its formula is not printed there).  Reading taken: the standard
+ * AddRmsNorm applied to the combine's bf16 output c (ep_combine, same
+ * arguments y .. num_shared):
+ *   x[s,t,:]  = float32(c[s,t,:]) + float32(residual[s,t,:])   (float32 add)
+ *   rstd[s,t] = 1 / sqrt(sum_h x^2 / H + eps)                  (float32)
+ *   y[s,t,h]  = bf16( (x[s,t,h] * rstd[s,t]) * gamma[h] )
+ * residual [R*T, H] bf16 and gamma [H] bf16 (device, 16-byte aligned);
+ * norm_out [R*T, H] bf16 receives y; x_out [R*T, H] bf16 receives bf16(x)
+ * (NULL: not written); rstd_out [R*T] float32 (NULL: not written).  eps must
+ * be finite and >= 0.  The combine's own output is not written.  Capacity and
+ * errors as for ep_combine. */
+ep_status ep_combine_add_rms_norm(const ep_handle* handle, const void* y, int64_t y_rows_capacity,
+                                  const float* topk_weights, const void* shared, int32_t num_shared,
+                                  const void* residual, const void* gamma, float eps, void* norm_out,
+                                  void* x_out, float* rstd_out, ep_stream_t stream);
+
 /* Writable device arrays of one layout, for ep_layout_static_scratch.  Shapes
  * as in ep_layout_views; status is one int32 word (the sticky status word). */
 typedef struct ep_layout_outputs {

@@ -240,3 +240,26 @@ def test_dispatch_ex_validation():
     st, h, _ = _create_fake(p)
     assert L.ep_dispatch_ex(h, A, D, 2, None, 0, PRE, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED
     ep.ep_handle_destroy(h)
+
+
+def test_combine_add_rms_norm_validation():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C, D, E_ = 1 << 40, 1 << 41, 1 << 42, 1 << 43, 1 << 44
+    nan = float("nan")
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, None, D, 1e-6, E_, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # no residual
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, None, 1e-6, E_, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # no gamma
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, D + 8, 1e-6, E_, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # unaligned gamma
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, D, -1.0, E_, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # negative eps
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, D, nan, E_, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # NaN eps
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, D, 1e-6, None, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # no output
+    assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, D, 1e-6, E_, E_ + 2, None, None) \
+        == ep.EP_ERR_INVALID_ARG                                                            # unaligned x_out
+    ep.ep_handle_destroy(h)

@@ -1,0 +1,126 @@
+"""GPU parity for the combine fused with the residual add and RMSNorm (CANN
+aclnnMoeDistributeCombineAddRmsNorm) against the oracle.
+
+- x_out, rstd and y within the tolerance derived in the oracle (combine
+  rounded to bf16, residual added and normalised in float32) of the float64
+  reference built from the oracle's own layout, dispatch and stand-in expert;
+- the composition: x_out equals, bit for bit, bf16(float32(c) + residual) with
+  c the plain combine's output of the same kernel arithmetic;
+- edges: no tokens, tokens without experts, a receive buffer that is too small;
+- full size (8 ranks x 4096 tokens, H = 7168, 256 experts, top-8): sampled
+  tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_layout_03_gb300 import ep, synth
+from gpu_harness import GpuRun, bf16_bits, oracle_combine_sampled, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+EPS = synth.RMS_NORM_EPS
+
+
+def run_norm(w, quant=0, mark=4, check_composition=True):
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    x = synth.gen_x(w)
+    shared = synth.gen_shared(w)
+    res = synth.gen_residual(w)
+    gam = synth.gen_gamma(w)
+    olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    g = GpuRun(w, topk)
+    x_dev = to_dev_bf16(x)
+    data, scales = g.dispatch(x_dev, quant)
+    y = g.expert(quant, data, scales, mark)
+    wts_dev = torch.from_numpy(wts).cuda()
+    sh_dev = None if shared is None else to_dev_bf16(shared)
+    res_dev = to_dev_bf16(res).view(w.N, w.H)
+    gam_dev = to_dev_bf16(gam)
+    out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device="cuda")
+    x_out = torch.empty_like(out)
+    rstd = torch.empty(w.N, dtype=torch.float32, device="cuda")
+    g.lay.combine_add_rms_norm(y, wts_dev, res_dev, gam_dev, out, x_out, rstd, sh_dev, EPS)
+    assert g.lay.status() == ep.EP_OK
+    # oracle: its own dispatch and stand-in expert, float64 combine and AddRmsNorm
+    od, os_ = oracle.dispatch(olay, x, quant)
+    rows = np.arange(olay.rows, dtype=np.int64)
+    oy = oracle.expert_rows(olay, rows, w.H, quant, od, os_, mark)
+    ref = oracle.combine_add_rms_norm_ref64(olay, oy, wts, shared, res, gam, EPS)
+    ok, worst = oracle.add_rms_norm_within_tolerance(bf16_bits(x_out), rstd.cpu().numpy(), bf16_bits(out),
+                                                     ref, w.K, w.num_shared)
+    assert ok, worst
+    if check_composition:
+        c = g.combine(y, wts_dev, sh_dev)
+        xf = (c.float() + res_dev.float()).to(torch.bfloat16)
+        assert torch.equal(xf.view(torch.int16), x_out.view(torch.int16))
+    return worst
+
+
+@pytest.mark.parametrize("idx,T,quant", [(1, 64, 0), (1, 64, 4), (2, 48, 0), (3, 40, 2), (5, 12, 0)])
+def test_combine_add_rms_norm_against_oracle(idx, T, quant):
+    w = synth.WORKLOADS[idx].with_(T=T)
+    if idx == 1:
+        w = w.with_(H=1024)
+    run_norm(w, quant)
+
+
+def test_ragged_hidden_and_chunks():
+    # H = 520: 65 vectors, a chunk size that does not divide the row
+    w = synth.WORKLOADS[1].with_(T=33, H=520, K=2)
+    run_norm(w)
+
+
+def test_edges():
+    # tokens without experts: x = shared sum + residual
+    w = synth.WORKLOADS[5].with_(T=9, drop_p=1.0)
+    run_norm(w)
+    # no tokens at all: nothing to do
+    w0 = synth.WORKLOADS[1].with_(T=0, H=256)
+    g = GpuRun(w0, np.zeros((w0.R, 0, w0.K), np.int64))
+    e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    g.lay.combine_add_rms_norm(e, torch.empty((0, w0.K), device="cuda"), e, torch.ones(256, dtype=torch.bfloat16,
+                               device="cuda"), e)
+    assert g.lay.status() == ep.EP_OK
+    # expert outputs shorter than the layout: capacity error, nothing written
+    w = synth.WORKLOADS[1].with_(H=256)
+    topk = synth.gen_topk(w)
+    g = GpuRun(w, topk)
+    y = torch.zeros((g.rows - 1, w.H), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((w.N, w.H), 3.0, dtype=torch.bfloat16, device="cuda")
+    res = torch.zeros((w.N, w.H), dtype=torch.bfloat16, device="cuda")
+    g.lay.combine_add_rms_norm(y, torch.ones((w.N, w.K), device="cuda"), res,
+                               torch.ones(w.H, dtype=torch.bfloat16, device="cuda"), out)
+    assert g.lay.status() == ep.EP_ERR_CAPACITY
+    assert torch.all(out == 3.0)
+
+
+def test_full_size_workload2_sampled():
+    w = synth.WORKLOADS[2]
+    rng = np.random.default_rng(12)
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    g = GpuRun(w, topk)
+    x_dev = synth.gen_x_device(w)
+    x = bf16_bits(x_dev).reshape(w.N, w.H)
+    data, _ = g.dispatch(x_dev, 0)
+    y = data.view(torch.bfloat16).view(-1, w.H)
+    res_dev = synth.gen_residual_device(w).view(w.N, w.H)
+    gam = synth.gen_gamma(w)
+    out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device="cuda")
+    x_out = torch.empty_like(out)
+    rstd = torch.empty(w.N, dtype=torch.float32, device="cuda")
+    g.lay.combine_add_rms_norm(y, torch.from_numpy(wts).cuda(), res_dev, to_dev_bf16(gam), out, x_out, rstd,
+                               None, EPS)
+    assert g.lay.status() == ep.EP_OK
+    tokens = np.unique(np.concatenate([rng.integers(0, w.N, 300), [0, w.N - 1]]))
+    _, c, mag = oracle_combine_sampled(olay, x, wts, None, 0, 0, tokens)
+    tk = torch.from_numpy(tokens).cuda()
+    xr, rs, yv = oracle.add_rms_norm_ref64(c, bf16_bits(res_dev[tk]), gam, EPS)
+    ref = dict(c=c, mag=mag, x=xr, rstd=rs, y=yv, gamma=oracle.bf16_bits_to_f64(gam))
+    ok, worst = oracle.add_rms_norm_within_tolerance(bf16_bits(x_out[tk]), rstd[tk].cpu().numpy(),
+                                                     bf16_bits(out[tk]), ref, w.K, 0)
+    assert ok, worst
