@@ -56,11 +56,15 @@ WORKLOAD_KEYS = {"1": (1, 0, 0, 0, "expert", ""), "2": (2, 0, 0, 0, "expert", ""
                  # alternate formats
                  "4p": (4, 4, 0, 0, "expert", "pre"), "4x": (4, 4, 0, 0, "expert", "bm"),
                  # combine fused with the residual add and RMSNorm
-                 "2n": (2, 0, 0, 0, "expert", "norm")}
+                 "2n": (2, 0, 0, 0, "expert", "norm"),
+                 # two-phase form (send, then wait) of dispatch and combine
+                 "2a": (2, 0, 0, 0, "expert", "split")}
 FORMAT = {"": "bf16 input, row-major scales",
           "pre": "pre-encoded (data, scale) rows moved unchanged",
           "bm": "block-major scales (blocks, capacity)",
-          "norm": "combine + residual add + RMSNorm (outputs y, x = combine + residual, rstd)"}
+          "norm": "combine + residual add + RMSNorm (outputs y, x = combine + residual, rstd)",
+          "split": "two-phase: dispatch send (per-rank arrival rows) + wait (grouped rows); "
+                   "combine send (token-major return slots) + wait (weighted sum)"}
 QNAME = {0: "none", 1: "int8_static", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "mxfp8_e5m2",
          6: "mxfp4_e2m1", 7: "fp8_e4m3_per_token", 8: "fp8_e5m2_per_token",
          9: "fp8_e4m3_per_group128", 10: "fp8_e5m2_per_group128"}
@@ -220,7 +224,7 @@ def make_inputs(w, device):
     return topk, wts, x_dev, sh_dev
 
 
-def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt=""):
+def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt="", trows=0):
     """Bytes each kernel must move (reads + writes).  Expert layout: V gathered
     rows in combine; per-rank layout: every receive row is gathered once (unit
     weights, no weight reads).  Pre-encoded input: the encoded rows are read
@@ -232,6 +236,13 @@ def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt=""):
     if fmt == "pre":
         disp = N * (db + sb) + N * K * 4 + rows * (db + sb) + (rows * 4 if sb else 0)
     norm = N * H * 2 * 3 + H * 2 + N * 4 if fmt == "norm" else 0   # residual in; x, rstd out
+    if fmt == "split":
+        # send: x in, arrival rows out; wait: V arrival rows in, grouped rows out
+        disp = N * H * 2 + N * K * 4 + trows * (db + sb) + V * (db + sb) + rows * (db + sb) + rows * 4
+        # send: V expert rows in, V slots out; wait: V slots in, N rows out
+        comb = 3 * V * H * 2 + N * K * 8 + S * N * H * 2 + N * H * 2
+        lay = N * K * 8 * 3 + N * K * 4 + rows * 4 + N * w.R + N * K * (8 + 4 + 4) + trows * (4 + K * 12)
+        return {"layout": lay, "dispatch": disp, "combine": comb}
     lay = N * K * 8 * 3 + N * K * 4 + rows * 4 + N * w.R
     if per_rank:
         comb = rows * H * 2 + N * K * 4 + S * N * H * 2 + N * H * 2
@@ -259,11 +270,18 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
     lay = ep.EPLayout(w.R, w.T, w.H, w.E, w.K, w.alpha, device=dev)
     lay.layout(topk_dev, active_mask=mask_dev)
     per_rank = recv_layout == "rank"
+    split = fmt == "split"
+    trows = 0
     if per_rank:
         ridx, rw = lay.token_layout(topk_dev, w_dev, active_mask=mask_dev)
         rows = int(lay.token_rows()[-1])
     else:
         rows = int(lay.recv_rows()[-1])
+    if split:
+        ridx, rw = lay.token_layout(topk_dev, w_dev, active_mask=mask_dev)
+        trows = int(lay.token_rows()[-1])
+        tok_data, tok_scales = lay.alloc_recv(quant, max(trows, 1), device=dev)
+        ret = lay.alloc_return(device=dev)
     V = int((topk >= 0).sum()) if mask_dev is None else None
     data, scales = lay.alloc_recv(quant, max(rows, 1), device=dev)
     scales_rm = scales
@@ -277,7 +295,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
 
     def do_layout(topk_t, w_t, s=None):
         lay.layout(topk_t, s, active_mask=mask_dev)
-        if per_rank:
+        if per_rank or split:
             lay.token_layout(topk_t, w_t, active_mask=mask_dev, stream=s, out=(ridx, rw))
 
     norm = fmt == "norm"
@@ -290,7 +308,10 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         res_dev = None
 
     def do_dispatch(x_t, s=None, xs_t=None):
-        if fmt in ("pre", "bm"):
+        if split:
+            lay.dispatch_async(x_t, quant, tok_data, tok_scales, s)
+            lay.dispatch_wait(quant, tok_data, tok_scales, data, scales, s)
+        elif fmt in ("pre", "bm"):
             lay.dispatch_ex(x_t, quant, data, scales, s, x_scales=xs_t, per_rank=per_rank,
                             pre_encoded=fmt == "pre", block_major=fmt == "bm")
         elif per_rank:
@@ -299,7 +320,10 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
             lay.dispatch(x_t, quant, data, scales, s, scales=sc_dev, scale_kind=kind)
 
     def do_combine(w_t, out_t, sh_t, s=None, res_t=None):
-        if norm:
+        if split:
+            lay.combine_async(y, ret, s)
+            lay.combine_wait(ret, w_t, out_t, sh_t, s)
+        elif norm:
             lay.combine_add_rms_norm(y, w_t, res_t if res_t is not None else res_dev, gamma_dev, out_t,
                                      x_out_dev, rstd_dev, sh_t, synth.RMS_NORM_EPS, s)
         elif per_rank:
@@ -307,7 +331,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         else:
             lay.combine(y, w_t, out_t, sh_t, s)
 
-    if quant == 0 and fmt in ("", "norm"):
+    if quant == 0 and fmt in ("", "norm", "split"):
         y = data.view(torch.bfloat16).view(-1, w.H)
     elif fmt:
         # expert outputs from the fused row-major path of the same bf16 x
@@ -445,12 +469,12 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         e2e_ms = s2.elapsed_time(t2) / k2
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h, "steps": k2}
         assert lay.status() == ep.EP_OK
-        if quant == 0 and fmt in ("", "norm"):
+        if quant == 0 and fmt in ("", "norm", "split"):
             # the copied-back output of the last step equals the device-resident result
             assert torch.equal(out_host[(k2 - 1) % 2].to(dev), out)
 
     clocks = sampler.summary(t_timed0, t_timed1, t_warm0)
-    bytes_ = algorithmic_bytes(w, quant, rows, V, per_rank, fmt)
+    bytes_ = algorithmic_bytes(w, quant, rows, V, per_rank, fmt, trows)
     return dict(total_ms=total_ms, phase=phase, e2e=e2e, clocks=clocks, bytes=bytes_, rows=rows,
                 V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_bf16, sh_dev=sh_dev)
 
@@ -512,6 +536,22 @@ def host_shared_lead(sh_dev, w, ranks=2):
 
 
 # --------------------------------------------------------------------- main
+
+def launches_per_step(quant, recv_layout, fmt):
+    """Kernels of this library launched per step: layout 3 (count, scan,
+    assign), dispatch 1, combine 1; the per-rank layout adds 2 (scan, assign);
+    the two-phase form adds a wait kernel to each exchange; a scale gather
+    follows the dispatch for pre-encoded rows with scales and for block-major
+    MX / per-group scales."""
+    n = 5
+    if recv_layout == "rank" or fmt == "split":
+        n += 2
+    if fmt == "split":
+        n += 2
+    if (fmt == "pre" and quant not in (0, 1)) or (fmt == "bm" and quant in (4, 5, 6, 9, 10)):
+        n += 1
+    return n
+
 
 def workload_config(w, quant, key, kind=0, mask_dims=0):
     return {"workload": f"ep_layout_dispatch_combine[{key}] " + w.name,
@@ -590,7 +630,7 @@ def main(argv=None):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (7 if recv_layout == "rank" else 5) * K,
+        "gpu_launches": launches_per_step(quant, recv_layout, fmt) * K,
         "clocks": res["clocks"],
         "kernels": {
             k: {"avg_ms": round(avg[k], 5), "median_ms": round(med[k], 5),

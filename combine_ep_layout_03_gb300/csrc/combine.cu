@@ -103,7 +103,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
     float* xbuf = red + 64;                                       // NORM: [H]
     uint16_t* gbuf = reinterpret_cast<uint16_t*>(xbuf + a.H);     // NORM: gamma [H]
     const int total = a.expert_base[a.E];
-    if ((int64_t)total > a.cap) {
+    if (!a.slot_rows && (int64_t)total > a.cap) {   // return slots are sized R*T*K by the caller
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
         return;
     }
@@ -137,6 +137,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
         if (cnt > 0 && lane < a.K) {
             const int64_t n = blockIdx.x;
             dn = a.dst_row[n * a.K + lane];
+            if (a.slot_rows && dn >= 0) dn = (int)(n * a.K + lane);
             wn = a.w ? a.w[n * a.K + lane] : 1.0f;   // null weights: unit (per-rank rows)
         }
         bool ok = true;
@@ -147,6 +148,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
             if (j + 1 < cnt && lane < a.K) {
                 const int64_t nn = n + G;
                 dn = a.dst_row[nn * a.K + lane];
+                if (a.slot_rows && dn >= 0) dn = (int)(nn * a.K + lane);
                 wn = a.w ? a.w[nn * a.K + lane] : 1.0f;
             }
             const unsigned mask = __ballot_sync(0xffffffffu, d >= 0);

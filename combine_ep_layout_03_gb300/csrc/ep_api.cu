@@ -382,6 +382,101 @@ ep_status ep_dispatch_ex(const ep_handle* hc, const void* x, const void* x_scale
                          flags);
 }
 
+ep_status ep_dispatch_async(const ep_handle* hc, const void* x, ep_quant_mode q, const float* scales,
+                            ep_scale_kind kind, void* tok_data, void* tok_scales, int64_t tok_cap,
+                            ep_stream_t stream) {
+    if (kind == EP_SCALES_PER_EXPERT) return EP_ERR_UNSUPPORTED;
+    return dispatch_impl(hc, x, q, scales, kind, tok_data, tok_scales, tok_cap, stream, true);
+}
+
+ep_status ep_dispatch_wait(const ep_handle* hc, ep_quant_mode q, const void* tok_data, const void* tok_scales,
+                           int64_t tok_cap, uint32_t flags, void* recv_data, void* recv_scales, int64_t cap,
+                           ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    if (flags & ~(uint32_t)EP_DISPATCH_SCALES_BLOCK_MAJOR) return EP_ERR_INVALID_ARG;
+    int64_t db = 0, sb = 0;
+    ep_status s = ep_recv_row_bytes(h->H, q, &db, &sb);
+    if (s != EP_OK) return s;
+    if (tok_cap < 0 || cap < 0) return EP_ERR_INVALID_ARG;
+    if (tok_cap > 0 && (!tok_data || !aligned_to(tok_data, 16))) return EP_ERR_INVALID_ARG;
+    if (cap > 0 && (!recv_data || !aligned_to(recv_data, 16))) return EP_ERR_INVALID_ARG;
+    if (sb > 0 && tok_cap > 0 && (!tok_scales || !aligned_to(tok_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (sb > 0 && cap > 0 && (!recv_scales || !aligned_to(recv_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    ExpandArgs a;
+    a.tok_data = (const uint8_t*)tok_data;
+    a.tok_scales = sb ? (const uint8_t*)tok_scales : nullptr;
+    a.data = (uint8_t*)recv_data;
+    a.scales = sb ? (uint8_t*)recv_scales : nullptr;
+    a.recv_src = h->recv_src;
+    a.rank_base = h->rank_base;
+    a.tok_base = h->tok_base;
+    a.tok_dst = h->tok_dst;
+    a.expert_base = h->expert_base;
+    a.tok_meta = h->tok_meta;
+    a.status = h->status;
+    a.cap = cap;
+    a.tok_cap = tok_cap;
+    a.rows_hint = cap;
+    a.R = h->R; a.E = h->E; a.K = h->K;
+    a.row_bytes = (int32_t)db;
+    a.scale_bytes = (int32_t)sb;
+    a.scales_t = (flags & EP_DISPATCH_SCALES_BLOCK_MAJOR) ? 1 : 0;
+    a.scale_elem = is_mx(q) ? 1 : 4;
+    return from_cuda(launch_expand_rows(h, a, (cudaStream_t)stream));
+}
+
+ep_status ep_combine_async(const ep_handle* hc, const void* y, int64_t y_cap, void* ret, int64_t ret_cap,
+                           ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (y_cap < 0 || ret_cap < h->N * h->K) return EP_ERR_INVALID_ARG;
+    if (h->N > 0) {
+        if (!ret || !aligned_to(ret, 16)) return EP_ERR_INVALID_ARG;
+        if (y_cap > 0 && (!y || !aligned_to(y, 16))) return EP_ERR_INVALID_ARG;
+    }
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    ReturnArgs a;
+    a.y = (const uint16_t*)y;
+    a.ret = (uint16_t*)ret;
+    a.dst_row = h->dst_row;
+    a.expert_base = h->expert_base;
+    a.status = h->status;
+    a.y_cap = y_cap;
+    a.slots = h->N * h->K;
+    a.H = h->H; a.E = h->E;
+    return from_cuda(launch_return_rows(h, a, (cudaStream_t)stream));
+}
+
+ep_status ep_combine_wait(const ep_handle* hc, const void* ret, int64_t ret_cap, const float* w,
+                          const void* shared, int32_t S, void* out, ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (S < 0 || S > kMaxShared || (S > 0 && (!shared || !aligned_to(shared, 16)))) return EP_ERR_INVALID_ARG;
+    if (ret_cap < h->N * h->K) return EP_ERR_INVALID_ARG;
+    if (h->N > 0) {
+        if (!w || !aligned_to(w, 4) || !out || !aligned_to(out, 16)) return EP_ERR_INVALID_ARG;
+        if (!ret || !aligned_to(ret, 16)) return EP_ERR_INVALID_ARG;
+    }
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    CombineArgs a;
+    a.y = (const uint16_t*)ret;
+    a.w = w;
+    a.shared = (const uint16_t*)shared;
+    a.out = (uint16_t*)out;
+    a.dst_row = h->dst_row;
+    a.expert_base = h->expert_base;
+    a.status = h->status;
+    a.N = h->N;
+    a.cap = ret_cap;
+    a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
+    a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
+    a.slot_rows = 1;
+    return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
+}
+
 ep_status ep_token_layout(ep_handle* h, const int64_t* topk, const float* w, const uint8_t* mask,
                           int32_t mask_dims, int64_t* recv_topk_idx, float* recv_topk_weights,
                           int64_t rows_cap, ep_stream_t stream) {
@@ -443,6 +538,7 @@ ep_status ep_combine_tokens(const ep_handle* hc, const void* y, int64_t y_cap, c
     a.cap = y_cap;
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = 1; a.S = S; a.nvec = h->H / 8;
     a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
+    a.slot_rows = 0;
     cudaError_t err = launch_combine(h, a, (cudaStream_t)stream);
     if (err == cudaSuccess && rank_w && out_w)
         err = launch_reduce_token_weights(h, rank_w, out_w, y_cap, (cudaStream_t)stream);
@@ -501,6 +597,7 @@ ep_status ep_combine(const ep_handle* hc, const void* y, int64_t y_cap, const fl
     a.cap = y_cap;
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
     a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
+    a.slot_rows = 0;
     return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
 }
 
@@ -537,6 +634,7 @@ ep_status ep_combine_add_rms_norm(const ep_handle* hc, const void* y, int64_t y_
     a.eps = eps;
     a.x_out = (uint16_t*)x_out;
     a.rstd = rstd_out;
+    a.slot_rows = 0;
     return from_cuda(launch_combine_norm(h, a, (cudaStream_t)stream));
 }
 

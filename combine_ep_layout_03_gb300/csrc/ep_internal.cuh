@@ -154,6 +154,37 @@ struct CombineArgs {
     float eps;
     uint16_t* x_out;          // [N][H] bf16(x), or null
     float* rstd;              // [N], or null
+    // Combine wait of the two-phase form: y holds token-major return slots,
+    // entry (n, k) reads slot n*K + k (when valid) instead of dst_row.
+    int32_t slot_rows;
+};
+
+// Dispatch wait: per-rank arrival rows -> per-expert (grouped) receive rows.
+struct ExpandArgs {
+    const uint8_t* tok_data;    // [tok_cap][row_bytes] arrival rows
+    const uint8_t* tok_scales;  // [tok_cap][scale_bytes] or null
+    uint8_t* data;              // [cap][row_bytes]
+    uint8_t* scales;            // [cap][scale_bytes], block-major [nb][cap], or null
+    const int32_t* recv_src;
+    const int64_t* rank_base;
+    const int64_t* tok_base;
+    const int32_t* tok_dst;
+    const int32_t* expert_base;
+    const int32_t* tok_meta;
+    int32_t* status;
+    int64_t cap, tok_cap, rows_hint;
+    int32_t R, E, K, row_bytes, scale_bytes, scales_t, scale_elem;
+};
+
+// Combine send: expert outputs -> token-major return slots.
+struct ReturnArgs {
+    const uint16_t* y;          // [y_cap][H]
+    uint16_t* ret;              // [slots][H]
+    const int32_t* dst_row;     // [slots]
+    const int32_t* expert_base;
+    int32_t* status;
+    int64_t y_cap, slots;
+    int32_t H, E;
 };
 
 struct IdentityArgs {
@@ -181,6 +212,8 @@ cudaError_t launch_identity(const ep_handle* h, const IdentityArgs& a, int quant
 cudaError_t launch_token_layout(const ep_handle* h, const TokenLayoutArgs& a, cudaStream_t st);
 cudaError_t launch_reduce_token_weights(const ep_handle* h, const float* rank_w, float* out_w,
                                         int64_t cap, cudaStream_t st);
+cudaError_t launch_expand_rows(const ep_handle* h, const ExpandArgs& a, cudaStream_t st);
+cudaError_t launch_return_rows(const ep_handle* h, const ReturnArgs& a, cudaStream_t st);
 cudaError_t launch_identity_tokens(const ep_handle* h, const IdentityArgs& a, const int64_t* ridx,
                                    const float* rw, int quant, cudaStream_t st);
 

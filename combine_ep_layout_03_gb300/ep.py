@@ -99,6 +99,10 @@ def _load():
         "ep_expert_identity_tokens": ([vp, st, vp, vp, vp, vp, i64, i32, vp, vp], st),
         "ep_dispatch_ex": ([vp, vp, vp, st, vp, st, ctypes.c_uint32, vp, vp, i64, vp], st),
         "ep_combine_add_rms_norm": ([vp, vp, i64, vp, vp, i32, vp, vp, ctypes.c_float, vp, vp, vp, vp], st),
+        "ep_dispatch_async": ([vp, vp, st, vp, st, vp, vp, i64, vp], st),
+        "ep_dispatch_wait": ([vp, st, vp, vp, i64, ctypes.c_uint32, vp, vp, i64, vp], st),
+        "ep_combine_async": ([vp, vp, i64, vp, i64, vp], st),
+        "ep_combine_wait": ([vp, vp, i64, vp, vp, i32, vp, vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -227,6 +231,30 @@ def ep_combine_add_rms_norm(h: int, y, y_rows_capacity: int, topk_weights, share
                                         int(num_shared), _ptr(residual), _ptr(gamma), float(eps),
                                         _ptr(norm_out), _ptr(x_out), _ptr(rstd_out), _stream(stream)),
            "ep_combine_add_rms_norm")
+
+
+def ep_dispatch_async(h: int, x, quant: int, scales, scale_kind: int, tok_data, tok_scales,
+                      tok_rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_dispatch_async(h, _ptr(x), quant, _ptr(scales), int(scale_kind), _ptr(tok_data),
+                                  _ptr(tok_scales), int(tok_rows_capacity), _stream(stream)), "ep_dispatch_async")
+
+
+def ep_dispatch_wait(h: int, quant: int, tok_data, tok_scales, tok_rows_capacity: int, flags: int, recv_data,
+                     recv_scales, recv_rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_dispatch_wait(h, quant, _ptr(tok_data), _ptr(tok_scales), int(tok_rows_capacity), int(flags),
+                                 _ptr(recv_data), _ptr(recv_scales), int(recv_rows_capacity), _stream(stream)),
+           "ep_dispatch_wait")
+
+
+def ep_combine_async(h: int, y, y_rows_capacity: int, ret, ret_rows_capacity: int, stream=None) -> None:
+    _check(_lib.ep_combine_async(h, _ptr(y), int(y_rows_capacity), _ptr(ret), int(ret_rows_capacity),
+                                 _stream(stream)), "ep_combine_async")
+
+
+def ep_combine_wait(h: int, ret, ret_rows_capacity: int, topk_weights, shared, num_shared: int, out,
+                    stream=None) -> None:
+    _check(_lib.ep_combine_wait(h, _ptr(ret), int(ret_rows_capacity), _ptr(topk_weights), _ptr(shared),
+                                int(num_shared), _ptr(out), _stream(stream)), "ep_combine_wait")
 
 
 def ep_combine(h: int, y, y_rows_capacity: int, topk_weights, shared, num_shared: int, out,
@@ -414,6 +442,34 @@ class EPLayout:
         S = 0 if shared is None else shared.shape[1]
         cap = y.numel() // self.H
         ep_combine(self.h, y, cap, topk_weights, shared, S, out, stream)
+        return out
+
+    def dispatch_async(self, x, quant, tok_data, tok_scales, stream=None, scales=None,
+                       scale_kind=EP_SCALES_NONE) -> None:
+        """Send phase: rows into the per-rank arrival layout (after token_layout)."""
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        ep_dispatch_async(self.h, x, quant, scales, scale_kind, tok_data, tok_scales, tok_data.numel() // db,
+                          stream)
+
+    def dispatch_wait(self, quant, tok_data, tok_scales, recv_data, recv_scales, stream=None,
+                      block_major: bool = False) -> None:
+        """Wait phase: arrival rows -> per-expert grouped rows."""
+        db, _ = ep_recv_row_bytes(self.H, quant)
+        ep_dispatch_wait(self.h, quant, tok_data, tok_scales, tok_data.numel() // db,
+                         EP_DISPATCH_SCALES_BLOCK_MAJOR if block_major else 0, recv_data, recv_scales,
+                         recv_data.numel() // db, stream)
+
+    def alloc_return(self, device="cuda") -> torch.Tensor:
+        """Token-major return buffer of the two-phase combine, [R*T*K, H] bf16."""
+        return torch.empty((max(self.R * self.T * self.K, 1), self.H), dtype=torch.bfloat16, device=device)
+
+    def combine_async(self, y: torch.Tensor, ret: torch.Tensor, stream=None) -> None:
+        ep_combine_async(self.h, y, y.numel() // self.H, ret, ret.numel() // self.H, stream)
+
+    def combine_wait(self, ret: torch.Tensor, topk_weights: torch.Tensor, out: torch.Tensor,
+                     shared: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        S = 0 if shared is None else shared.shape[1]
+        ep_combine_wait(self.h, ret, ret.numel() // self.H, topk_weights, shared, S, out, stream)
         return out
 
     def combine_add_rms_norm(self, y: torch.Tensor, topk_weights: torch.Tensor, residual: torch.Tensor,

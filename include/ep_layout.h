@@ -378,6 +378,54 @@ ep_status ep_dispatch_ex(const ep_handle* handle, const void* x, const void* x_s
                          uint32_t flags, void* recv_data, void* recv_scales,
                          int64_t recv_rows_capacity, ep_stream_t stream);
 
+/* ---- Two-phase dispatch and combine (send, then wait) --------------------- */
+/* Modular MAX "EPBatchManager": ep_dispatch_async / ep_dispatch_wait and
+ * ep_combine_async / ep_combine_wait split each exchange into a phase that
+ * starts the transfers and a phase that waits for them and reorganises the
+ * received rows.  With all ranks on one GPU nothing is in flight between the
+ * phases: each is a kernel on the stream, and the buffer handed from one
+ * phase to the next stands for the receiving ranks' buffers.  Composed, each
+ * pair gives exactly the result of the one-call form (ep_dispatch_scaled /
+ * ep_combine), at the cost of writing and reading that buffer. */
+
+/* Device.  Dispatch send phase: every token's row, encoded once, is written
+ * once per destination rank into that rank's arrival rows: the per-rank
+ * layout of ep_token_layout, which must have run on the same stream after
+ * ep_layout.  Arguments and errors as for ep_dispatch_tokens. */
+ep_status ep_dispatch_async(const ep_handle* handle, const void* x, ep_quant_mode quant,
+                            const float* scales, ep_scale_kind scale_kind, void* tok_data,
+                            void* tok_scales, int64_t tok_rows_capacity, ep_stream_t stream);
+
+/* Device.  Dispatch wait phase: organises the arrival rows (tok_data /
+ * tok_scales written by ep_dispatch_async, tok_rows_capacity rows) into the
+ * per-expert grouped layout of ep_layout: receive row r of expert e (on rank
+ * j) copies the arrival row of its source token on rank j; padding rows get
+ * zero bytes.  recv_data / recv_scales as for ep_dispatch; flags may hold
+ * EP_DISPATCH_SCALES_BLOCK_MAJOR.  Capacity overflow (either buffer) sets
+ * EP_ERR_CAPACITY and writes nothing; an arrival row missing from the
+ * per-rank layout (layouts of different routings) sets EP_ERR_INVALID_ARG in
+ * the status word. */
+ep_status ep_dispatch_wait(const ep_handle* handle, ep_quant_mode quant, const void* tok_data,
+                           const void* tok_scales, int64_t tok_rows_capacity, uint32_t flags,
+                           void* recv_data, void* recv_scales, int64_t recv_rows_capacity,
+                           ep_stream_t stream);
+
+/* Device.  Combine send phase: the expert output of every valid entry
+ * (s,t,k), row dst_row[s,t,k] of y [y_rows_capacity, H] bf16, is copied
+ * unweighted into slot (s*T + t)*K + k of the token-major return buffer ret
+ * [ret_rows_capacity >= R*T*K, H] bf16 (16-byte aligned).  Slots of invalid
+ * entries are not written.  Capacity of y as for ep_combine. */
+ep_status ep_combine_async(const ep_handle* handle, const void* y, int64_t y_rows_capacity, void* ret,
+                           int64_t ret_rows_capacity, ep_stream_t stream);
+
+/* Device.  Combine wait phase: out[s,t,:] = bf16( sum_k w[s,t,k] *
+ * ret[(s*T+t)*K + k, :] + sum_q shared[s,q,t,:] ) over the valid entries,
+ * float32 accumulation in the order of ep_combine (so the result equals
+ * ep_combine's bit for bit).  Arguments as for ep_combine. */
+ep_status ep_combine_wait(const ep_handle* handle, const void* ret, int64_t ret_rows_capacity,
+                          const float* topk_weights, const void* shared, int32_t num_shared, void* out,
+                          ep_stream_t stream);
+
 /* ---- Combine with residual add and RMSNorm -------------------------------- */
 
 /* Device.  CANN's aclnnMoeDistributeCombineAddRmsNorm (named on the

@@ -331,6 +331,30 @@ def dispatch_bytes(lay, src_rows: np.ndarray, rows: int | None = None) -> np.nda
     return out
 
 
+def return_slots(lay, y_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Combine send phase of the two-phase form (MAX ep_combine_async): slot
+    (s*T + t)*K + k of a token-major buffer holds the expert output row
+    dst_row[s,t,k] of y (unweighted).  Returns (slots [R*T*K, H] bf16 bits,
+    valid mask [R*T*K]); invalid slots are zero here and unspecified on the
+    device."""
+    d = np.asarray(lay.dst_row).reshape(-1).astype(np.int64)
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    H = y.shape[-1]
+    y = y.reshape(-1, H)
+    valid = d >= 0
+    out = np.zeros((d.size, H), np.uint16)
+    out[valid] = y[d[valid]]
+    return out, valid
+
+
+def slot_layout(lay) -> Layout:
+    """The layout the combine wait phase reads: entry (s,t,k) at slot
+    (s*T + t)*K + k when valid, -1 otherwise."""
+    d = np.asarray(lay.dst_row).reshape(-1)
+    ids = np.where(d >= 0, np.arange(d.size), -1).astype(np.int32)
+    return Layout(R=lay.R, T=lay.T, K=lay.K, dst_row=ids.reshape(lay.R, lay.T, lay.K))
+
+
 def transpose_scales(scales_rows: np.ndarray, capacity: int, elem_bytes: int) -> np.ndarray:
     """Row-major receive scales [rows, nb * elem_bytes] (uint8) rearranged into
     the block-major layout of MAX ep_dispatch's output_scales, shape

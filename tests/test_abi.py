@@ -263,3 +263,21 @@ def test_combine_add_rms_norm_validation():
     assert L.ep_combine_add_rms_norm(h, A, 10, B, None, 0, C, D, 1e-6, E_, E_ + 2, None, None) \
         == ep.EP_ERR_INVALID_ARG                                                            # unaligned x_out
     ep.ep_handle_destroy(h)
+
+
+def test_two_phase_validation():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C, D = 1 << 40, 1 << 41, 1 << 42, 1 << 43
+    NK = 2 * 8 * 2
+    assert L.ep_dispatch_async(h, A, 2, C, 3, B, C, 10, None) == ep.EP_ERR_UNSUPPORTED       # per-expert
+    assert L.ep_dispatch_wait(h, 4, A, B, 10, 1, C, D, 10, None) == ep.EP_ERR_INVALID_ARG    # per-rank flag
+    assert L.ep_dispatch_wait(h, 4, A, None, 10, 0, C, D, 10, None) == ep.EP_ERR_INVALID_ARG  # no arrival scales
+    assert L.ep_dispatch_wait(h, 0, A + 8, None, 10, 0, C, None, 10, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch_wait(h, 11, A, None, 10, 0, C, None, 10, None) == ep.EP_ERR_UNSUPPORTED
+    assert L.ep_combine_async(h, A, 10, B, NK - 1, None) == ep.EP_ERR_INVALID_ARG           # return too small
+    assert L.ep_combine_async(h, A, 10, B + 4, NK, None) == ep.EP_ERR_INVALID_ARG           # unaligned
+    assert L.ep_combine_wait(h, A, NK - 1, B, None, 0, C, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_combine_wait(h, A, NK, None, None, 0, C, None) == ep.EP_ERR_INVALID_ARG     # no weights
+    ep.ep_handle_destroy(h)

@@ -10,6 +10,11 @@ Block-major scales (Modular MAX "EPBatchManager", ep_dispatch returns: FP8
 output_scales of shape (hidden // block_size, max_recv_tokens)): element b of
 receive row r sits at [b, r].  Pinned by hand-written examples and by the
 identity that reading it back column by column gives the row-major scales.
+
+Two-phase form (Modular MAX ep_dispatch_async / wait, ep_combine_async /
+wait): the return slots against brute force, the wait phase over them equal
+to the one-call combine, and the arrival rows of the per-rank layout expanded
+by the grouped layout equal to the fused dispatch.
 """
 import numpy as np
 import pytest
@@ -99,3 +104,51 @@ def test_transpose_scales_reads_back(elem):
         for b in range(nb):
             assert np.array_equal(t[b, r], s[r, b * elem:(b + 1) * elem])
     assert not t[:, rows:].any()
+
+
+# ---- two-phase form (MAX ep_dispatch_async / wait, ep_combine_async / wait) ----
+
+def test_return_slots_brute_force_and_wait_equals_combine():
+    rng = np.random.default_rng(31)
+    R, T, E, K, H = 3, 5, 6, 3, 16
+    topk = rng.integers(-1, E, size=(R, T, K))
+    lay = oracle.layout(R, T, E, K, 2, topk)
+    y = rng.integers(0, 1 << 15, size=(max(lay.rows, 1), H), dtype=np.uint16)   # finite bf16 patterns
+    slots, valid = oracle.return_slots(lay, y)
+    for s in range(R):
+        for t in range(T):
+            for k in range(K):
+                i = (s * T + t) * K + k
+                d = int(lay.dst_row[s, t, k])
+                assert valid[i] == (d >= 0)
+                if d >= 0:
+                    assert np.array_equal(slots[i], y[d])
+    w = rng.random((R, T, K)).astype(np.float32)
+    # the wait phase over the slots reproduces the one-call combine exactly
+    assert np.array_equal(oracle.combine(oracle.slot_layout(lay), slots, w), oracle.combine(lay, y, w))
+
+
+def test_dispatch_wait_of_arrival_rows_equals_dispatch():
+    # arrival rows (per-rank layout) expanded by the grouped layout's rows are the fused dispatch
+    w = synth.WORKLOADS[1].with_(H=128, alpha=4, T=20)
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    x = synth.gen_x(w)
+    lay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    tl = oracle.token_layout(w.R, w.T, w.E, w.K, topk, wts)
+    for q in (oracle.Q_NONE, oracle.Q_E4M3, oracle.Q_INT8):
+        td, ts = oracle.token_dispatch(tl, x, q)
+        # per grouped row: the arrival row of its source token on its rank
+        rank_of_row = np.searchsorted(lay.rank_base, np.arange(lay.rows), side="right") - 1
+        src = lay.recv_src
+        d, s_ = oracle.dispatch(lay, x, q)
+        for r in range(lay.rows):
+            if src[r] < 0:
+                assert not d[r].any()
+                continue
+            j = rank_of_row[r]
+            p = [q_ for q_ in tl.tok_dst[src[r]] if tl.rank_tok_base[j] <= q_ < tl.rank_tok_base[j + 1]]
+            assert len(p) == 1
+            assert np.array_equal(td[p[0]], d[r])
+            if s_.shape[1]:
+                assert np.array_equal(ts[p[0]], s_[r])
