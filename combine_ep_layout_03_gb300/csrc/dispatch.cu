@@ -528,8 +528,10 @@ __device__ void zero_rows_part(const DispatchArgs& a, int64_t r0, int64_t r1, in
 // element c of receive row r takes element c of src row recv_src[r], and 0 for
 // a padding row.  Block-major: one receive row per thread, so for every block
 // b a warp stores 32 consecutive rows (one 32-byte run); the thread reads its
-// source row 16 bytes at a time when VEC.  Row-major: one receive row per
-// warp, lanes across the row.  The source rows are small and stay in L2.
+// source row 16 bytes at a time when VEC, four reads in flight before their
+// stores.  Row-major: a warp takes RU rows at once, lanes across the rows'
+// elements, so RU dependent source loads are in flight per lane.  The source
+// rows are small and stay in L2.
 template <int ES, bool VEC>
 __global__ void __launch_bounds__(256) scale_gather_kernel(DispatchArgs a, const uint8_t* src) {
     using T = typename std::conditional<ES == 4, uint32_t, uint8_t>::type;
@@ -549,16 +551,24 @@ __global__ void __launch_bounds__(256) scale_gather_kernel(DispatchArgs a, const
             }
             if constexpr (VEC) {
                 constexpr int PER = 16 / ES;
+                constexpr int VU = 4;
                 const uint4* srow = reinterpret_cast<const uint4*>(src + (int64_t)sr * a.scale_bytes);
-                for (int v = 0; v < nb / PER; ++v) {
-                    const uint4 q = __ldg(srow + v);
-                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                const int nvv = nb / PER;
+                for (int v0 = 0; v0 < nvv; v0 += VU) {
+                    uint4 q[VU];
 #pragma unroll
-                    for (int j = 0; j < PER; ++j) {
-                        T e;
-                        if constexpr (ES == 4) e = w[j];
-                        else e = (T)(w[j >> 2] >> (8 * (j & 3)));
-                        o[(int64_t)(v * PER + j) * a.cap] = e;
+                    for (int u = 0; u < VU; ++u) q[u] = v0 + u < nvv ? __ldg(srow + v0 + u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int u = 0; u < VU; ++u) {
+                        if (v0 + u >= nvv) break;
+                        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                        for (int j = 0; j < PER; ++j) {
+                            T e;
+                            if constexpr (ES == 4) e = w[j];
+                            else e = (T)(w[j >> 2] >> (8 * (j & 3)));
+                            o[(int64_t)((v0 + u) * PER + j) * a.cap] = e;
+                        }
                     }
                 }
             } else {
@@ -568,13 +578,22 @@ __global__ void __launch_bounds__(256) scale_gather_kernel(DispatchArgs a, const
             }
         }
     } else {
+        constexpr int RU = 8;
         const int lane = threadIdx.x & 31;
         const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-        for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total; r += warps) {
-            const int sr = a.recv_src[r];
-            T* o = out + r * nb;
-            const T* srow = s + (int64_t)(sr < 0 ? 0 : sr) * nb;
-            for (int c = lane; c < nb; c += 32) o[c] = sr >= 0 ? __ldg(srow + c) : T(0);
+        for (int64_t r0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RU; r0 < total;
+             r0 += warps * RU) {
+            int sr[RU];
+#pragma unroll
+            for (int u = 0; u < RU; ++u) sr[u] = r0 + u < total ? a.recv_src[r0 + u] : -1;
+            for (int c = lane; c < nb; c += 32) {
+                T v[RU];
+#pragma unroll
+                for (int u = 0; u < RU; ++u) v[u] = sr[u] >= 0 ? __ldg(s + (int64_t)sr[u] * nb + c) : T(0);
+#pragma unroll
+                for (int u = 0; u < RU; ++u)
+                    if (r0 + u < total) out[(r0 + u) * nb + c] = v[u];
+            }
         }
     }
 }
