@@ -511,7 +511,11 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
 #define EP_DISPATCH_LAG 4
 #endif
 #ifndef EP_DISPATCH_CTAS_PER_SM
-#define EP_DISPATCH_CTAS_PER_SM 1
+// Two issuing CTAs per SM: the same speed as one for 8-16 KB rows, 8 % faster
+// for 4 KB rows (pre-encoded MXFP8 at H = 4096), where one thread's per-row
+// issue overhead shows.  The ring still holds >= kTmaLag + 2 stages of the
+// largest row (H = 8192 bf16).
+#define EP_DISPATCH_CTAS_PER_SM 2
 #endif
 constexpr int kTmaLag = EP_DISPATCH_LAG;  // bulk-store groups allowed to read a stage
 constexpr int kDstSlotInts = 32;    // 128-byte slot per stage for the dst_row window
