@@ -131,6 +131,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
     const int rowb = c.CH * 2;
 
     if (warp == 0) {
+        if (a.stall_producer) return;   // tests of the bounded waits: nothing arrives
         // producer: lane k < K holds slot k of the current token (next one prefetched)
         int dn = -1;
         float wn = 0.0f;
@@ -159,7 +160,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
                 const int64_t q = j * c.nch + ci;
                 const int s = (int)(q % c.nstages);
                 const int64_t u = q / c.nstages;
-                if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), kMaxPolls)) ok = false;
+                if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), a.max_polls)) ok = false;
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 const int e0 = ci * c.CH;
                 const int ce = min(c.CH, a.H - e0);
@@ -200,7 +201,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
         const int ci = (int)(q - j * c.nch);
         const int64_t n = blockIdx.x + j * G;
         const int s = (int)(q % c.nstages);
-        if (!mbar_wait(&full[s], (uint32_t)((q / c.nstages) & 1), kMaxPolls)) { ok = false; break; }
+        if (!mbar_wait(&full[s], (uint32_t)((q / c.nstages) & 1), a.max_polls)) { ok = false; break; }
         const int32_t* m = meta + s * kMetaInts;
         const int kv = m[0];
         const int e0 = ci * c.CH;
@@ -255,7 +256,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
                     red[par * 32 + ((tid - 32) >> 5)] = t;
                     mbar_arrive(&redbar[par]);
                 }
-                if (!mbar_wait(&redbar[par], (uint32_t)((j >> 1) & 1), kMaxPolls)) { ok = false; break; }
+                if (!mbar_wait(&redbar[par], (uint32_t)((j >> 1) & 1), a.max_polls)) { ok = false; break; }
                 float sum = 0.0f;
                 for (int wi = 0; wi < ncw; ++wi) sum += red[par * 32 + wi];
                 const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, (float)a.H), a.eps)));

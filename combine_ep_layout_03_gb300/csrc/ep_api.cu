@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "ep_internal.cuh"
+#include "tma.cuh"
 
 namespace {
 
@@ -474,6 +475,7 @@ ep_status ep_combine_wait(const ep_handle* hc, const void* ret, int64_t ret_cap,
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
     a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
     a.slot_rows = 1;
+    a.max_polls = kMaxPolls; a.stall_producer = 0;
     return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
 }
 
@@ -539,6 +541,7 @@ ep_status ep_combine_tokens(const ep_handle* hc, const void* y, int64_t y_cap, c
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = 1; a.S = S; a.nvec = h->H / 8;
     a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
     a.slot_rows = 0;
+    a.max_polls = kMaxPolls; a.stall_producer = 0;
     cudaError_t err = launch_combine(h, a, (cudaStream_t)stream);
     if (err == cudaSuccess && rank_w && out_w)
         err = launch_reduce_token_weights(h, rank_w, out_w, y_cap, (cudaStream_t)stream);
@@ -598,6 +601,7 @@ ep_status ep_combine(const ep_handle* hc, const void* y, int64_t y_cap, const fl
     a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = S; a.nvec = h->H / 8;
     a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
     a.slot_rows = 0;
+    a.max_polls = kMaxPolls; a.stall_producer = 0;
     return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
 }
 
@@ -635,7 +639,37 @@ ep_status ep_combine_add_rms_norm(const ep_handle* hc, const void* y, int64_t y_
     a.x_out = (uint16_t*)x_out;
     a.rstd = rstd_out;
     a.slot_rows = 0;
+    a.max_polls = kMaxPolls; a.stall_producer = 0;
     return from_cuda(launch_combine_norm(h, a, (cudaStream_t)stream));
+}
+
+ep_status ep_test_combine_stalled(const ep_handle* hc, const void* y, int64_t y_cap, const float* w,
+                                  void* out, uint32_t max_polls, ep_stream_t stream) {
+    ep_handle* h = const_cast<ep_handle*>(hc);
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (max_polls < 1 || max_polls > kMaxPolls) return EP_ERR_INVALID_ARG;
+    if (y_cap < 0) return EP_ERR_INVALID_ARG;
+    if (h->N > 0) {
+        if (!w || !aligned_to(w, 4) || !out || !aligned_to(out, 16)) return EP_ERR_INVALID_ARG;
+        if (y_cap > 0 && (!y || !aligned_to(y, 16))) return EP_ERR_INVALID_ARG;
+    }
+    if (ep_device_sms(h) <= 0) return EP_ERR_CUDA;
+    CombineArgs a;
+    a.y = (const uint16_t*)y;
+    a.w = w;
+    a.shared = nullptr;
+    a.out = (uint16_t*)out;
+    a.dst_row = h->dst_row;
+    a.expert_base = h->expert_base;
+    a.status = h->status;
+    a.N = h->N;
+    a.cap = y_cap;
+    a.T = h->T; a.H = h->H; a.K = h->K; a.E = h->E; a.S = 0; a.nvec = h->H / 8;
+    a.residual = nullptr; a.gamma = nullptr; a.eps = 0.0f; a.x_out = nullptr; a.rstd = nullptr;
+    a.slot_rows = 0;
+    a.max_polls = max_polls;
+    a.stall_producer = 1;
+    return from_cuda(launch_combine(h, a, (cudaStream_t)stream));
 }
 
 ep_status ep_expert_identity(const ep_handle* hc, ep_quant_mode q, const void* recv_data,

@@ -157,6 +157,11 @@ struct CombineArgs {
     // Combine wait of the two-phase form: y holds token-major return slots,
     // entry (n, k) reads slot n*K + k (when valid) instead of dst_row.
     int32_t slot_rows;
+    // Polls of each bounded mbarrier wait before it gives up (kMaxPolls on
+    // the path).  stall_producer (tests of the bounded waits only): the
+    // producer warp issues nothing, so every consumer wait runs out.
+    uint32_t max_polls;
+    int32_t stall_producer;
 };
 
 // Dispatch wait: per-rank arrival rows -> per-expert (grouped) receive rows.

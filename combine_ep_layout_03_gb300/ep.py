@@ -99,6 +99,7 @@ def _load():
         "ep_expert_identity_tokens": ([vp, st, vp, vp, vp, vp, i64, i32, vp, vp], st),
         "ep_dispatch_ex": ([vp, vp, vp, st, vp, st, ctypes.c_uint32, vp, vp, i64, vp], st),
         "ep_combine_add_rms_norm": ([vp, vp, i64, vp, vp, i32, vp, vp, ctypes.c_float, vp, vp, vp, vp], st),
+        "ep_test_combine_stalled": ([vp, vp, i64, vp, vp, ctypes.c_uint32, vp], st),
         "ep_dispatch_async": ([vp, vp, st, vp, st, vp, vp, i64, vp], st),
         "ep_dispatch_wait": ([vp, st, vp, vp, i64, ctypes.c_uint32, vp, vp, i64, vp], st),
         "ep_combine_async": ([vp, vp, i64, vp, i64, vp], st),
@@ -231,6 +232,13 @@ def ep_combine_add_rms_norm(h: int, y, y_rows_capacity: int, topk_weights, share
                                         int(num_shared), _ptr(residual), _ptr(gamma), float(eps),
                                         _ptr(norm_out), _ptr(x_out), _ptr(rstd_out), _stream(stream)),
            "ep_combine_add_rms_norm")
+
+
+def ep_test_combine_stalled(h: int, y, y_rows_capacity: int, topk_weights, out, max_polls: int,
+                            stream=None) -> None:
+    """Test hook: the combine with a producer that issues nothing (bounded waits run out)."""
+    _check(_lib.ep_test_combine_stalled(h, _ptr(y), int(y_rows_capacity), _ptr(topk_weights), _ptr(out),
+                                        int(max_polls), _stream(stream)), "ep_test_combine_stalled")
 
 
 def ep_dispatch_async(h: int, x, quant: int, scales, scale_kind: int, tok_data, tok_scales,

@@ -446,6 +446,21 @@ ep_status ep_combine_add_rms_norm(const ep_handle* handle, const void* y, int64_
                                   const void* residual, const void* gamma, float eps, void* norm_out,
                                   void* x_out, float* rstd_out, ep_stream_t stream);
 
+/* ---- Test hook ------------------------------------------------------------ */
+
+/* Device.  For tests of the bounded waits only, never part of the path: runs
+ * the combine of ep_combine (no shared rows) with its producer warp issuing no
+ * copy, so every consumer's wait on a stage runs out after max_polls polls
+ * (1 <= max_polls <= 2^22; each poll may suspend the thread for a
+ * hardware-chosen interval).  The kernel then records EP_ERR_TIMEOUT in the
+ * status word and returns; nothing is in flight and the context stays
+ * usable (the next ep_layout clears the status word).  out is left as it
+ * was.  No page describes this: the pages' status codes cover host-visible
+ * errors only. */
+ep_status ep_test_combine_stalled(const ep_handle* handle, const void* y, int64_t y_rows_capacity,
+                                  const float* topk_weights, void* out, uint32_t max_polls,
+                                  ep_stream_t stream);
+
 /* Writable device arrays of one layout, for ep_layout_static_scratch.  Shapes
  * as in ep_layout_views; status is one int32 word (the sticky status word). */
 typedef struct ep_layout_outputs {

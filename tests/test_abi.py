@@ -281,3 +281,14 @@ def test_two_phase_validation():
     assert L.ep_combine_wait(h, A, NK - 1, B, None, 0, C, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_combine_wait(h, A, NK, None, None, 0, C, None) == ep.EP_ERR_INVALID_ARG     # no weights
     ep.ep_handle_destroy(h)
+
+
+def test_stalled_combine_hook_validation():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C = 1 << 40, 1 << 41, 1 << 42
+    assert L.ep_test_combine_stalled(h, A, 10, B, C, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_test_combine_stalled(h, A, 10, B, C, (1 << 22) + 1, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_test_combine_stalled(h, A, 10, None, C, 16, None) == ep.EP_ERR_INVALID_ARG
+    ep.ep_handle_destroy(h)
