@@ -21,7 +21,7 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-class GpuRun:
+class GpuPath:
     """Layout + dispatch (+ stand-in expert + combine) on the GPU."""
 
     def __init__(self, w: synth.Workload, topk: np.ndarray, recv_capacity_rows: int = 0):

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import synth
-from gpu_harness import GpuRun, bf16_bits, compare_layout, oracle_combine_sampled
+from gpu_harness import GpuPath, bf16_bits, compare_layout, oracle_combine_sampled
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_full_size(idx):
     topk = synth.gen_topk(w)
     wts = synth.gen_weights(w, topk)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     assert g.rows == olay.rows
     compare_layout(g.views_numpy(), olay)
     assert g.lay.status() == 0

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import synth
-from gpu_harness import (GpuRun, bf16_bits, compare_layout, oracle_combine_sampled, to_dev_bf16)
+from gpu_harness import (GpuPath, bf16_bits, compare_layout, oracle_combine_sampled, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,7 @@ def test_layout_dispatch_combine_reduced(idx, T):
     w = reduced(idx, T)
     topk, wts, x, shared = inputs(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     assert g.rows == olay.rows
     compare_layout(g.views_numpy(), olay)
     assert g.lay.status() == 0
@@ -91,7 +91,7 @@ def test_ragged_and_extreme_hidden(H, q):
     w = synth.Workload(11, R=4, T=50, H=H, E=16, K=3, alpha=4)
     topk, wts, x, _ = inputs(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     compare_layout(g.views_numpy(), olay)
     data, scales = g.dispatch(to_dev_bf16(x), q, fill=0x5A)
     od, os_ = check_dispatch(g, olay, x, q, data, scales)
@@ -105,7 +105,7 @@ def test_random_expert_outputs_combine():
     w = reduced(2, 128)
     topk, wts, _, _ = inputs(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     y_bits = synth.gen_y(w, olay.rows)
     out = g.combine(to_dev_bf16(y_bits), torch.from_numpy(wts).cuda())
     o = oracle.combine(olay, y_bits, wts)
@@ -122,7 +122,7 @@ def test_edge_tokens_without_experts_and_shared_only():
     topk[0, :5] = -1          # tokens with no expert at all
     wts = synth.gen_weights(w, topk)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     compare_layout(g.views_numpy(), olay)
     assert g.views_numpy()["is_token_in_rank"][0, :5].sum() == 0
     data, scales = g.dispatch(to_dev_bf16(x), 0)
@@ -135,7 +135,7 @@ def test_edge_tokens_without_experts_and_shared_only():
 def test_edge_T0_and_all_invalid():
     w = synth.Workload(13, R=3, T=0, H=64, E=6, K=2, alpha=4)
     topk = np.zeros((3, 0, 2), np.int64)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     assert g.rows == 0 and g.lay.status() == 0
     v = g.views_numpy()
     assert np.all(v["expert_start"] == 0) and np.all(v["rank_base"] == 0)
@@ -146,7 +146,7 @@ def test_edge_T0_and_all_invalid():
     w = synth.Workload(14, R=2, T=7, H=64, E=4, K=2, alpha=3)
     topk = -np.ones((2, 7, 2), np.int64)
     olay = oracle.layout(2, 7, 4, 2, 3, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     compare_layout(g.views_numpy(), olay)
     assert g.rows == 0
 
@@ -156,7 +156,7 @@ def test_edge_alignment_larger_than_counts_L1_K1():
         w = synth.Workload(15, R=R, T=37, H=128, E=E, K=K, alpha=alpha)
         topk, wts, x, _ = inputs(w)
         olay = oracle.layout(R, w.T, E, K, alpha, topk)
-        g = GpuRun(w, topk)
+        g = GpuPath(w, topk)
         compare_layout(g.views_numpy(), olay)
         data, scales = g.dispatch(to_dev_bf16(x), 2)
         check_dispatch(g, olay, x, 2, data, scales)
@@ -167,7 +167,7 @@ def test_edge_zipf_extreme_skew_all_to_expert0():
     topk = np.zeros((4, 300, 1), np.int64)
     topk[1, 7, 0] = 31
     olay = oracle.layout(4, 300, 32, 1, 128, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     compare_layout(g.views_numpy(), olay)
     x = synth.gen_x(w)
     data, scales = g.dispatch(to_dev_bf16(x), 4)
@@ -188,7 +188,7 @@ def test_zero_rows_and_special_blocks_quant():
     xf[6:] = np.random.default_rng(0).standard_normal((6, 64)) * 1e-3
     x = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(2, 6, 64)
     olay = oracle.layout(2, 6, 4, 2, 1, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     for q in (2, 4, 5, 6):
         data, scales = g.dispatch(to_dev_bf16(x), q)
         check_dispatch(g, olay, x, q, data, scales)
@@ -201,7 +201,7 @@ def test_bad_expert_id_sets_status_and_counts_as_invalid():
     topk[1, 5, 0] = -7
     olay = oracle.layout(2, 20, 4, 2, 1, topk)
     assert olay.status == 4
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     assert g.lay.status() == 4
     compare_layout(g.views_numpy(), olay)
 
@@ -211,14 +211,14 @@ def test_capacity_overflow_writes_nothing():
     topk, wts, x, _ = inputs(w)
     olay = oracle.layout(2, 30, 4, 2, 1, topk)
     # layout capacity below the rows needed
-    g = GpuRun(w, topk, recv_capacity_rows=olay.rows - 3)
+    g = GpuPath(w, topk, recv_capacity_rows=olay.rows - 3)
     assert g.lay.status() == 3
     # dispatch / combine capacity below the rows needed: buffers untouched
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     data, scales = g.dispatch(to_dev_bf16(x), 2, rows=olay.rows - 1, fill=0x77)
     assert g.lay.status() == 3
     assert torch.all(data == 0x77) and torch.all(scales == 0x77)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     y = torch.zeros((olay.rows - 1, 64), dtype=torch.bfloat16, device="cuda")
     out = torch.full((60, 64), 3.0, dtype=torch.bfloat16, device="cuda")
     g.lay.combine(y, torch.from_numpy(wts).cuda(), out)
@@ -230,7 +230,7 @@ def test_deterministic_across_runs():
     topk, wts, x, _ = inputs(w)
     res = []
     for _ in range(2):
-        g = GpuRun(w, topk)
+        g = GpuPath(w, topk)
         data, scales = g.dispatch(to_dev_bf16(x), 2)
         y = g.expert(2, data, scales, 0)
         out = g.combine(y, torch.from_numpy(wts).cuda())

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import GpuRun, bf16_bits, compare_layout, oracle_combine_sampled, to_dev_bf16
+from gpu_harness import GpuPath, bf16_bits, compare_layout, oracle_combine_sampled, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def run_case(w, q, kind, mark=16, check_combine=True):
     x = synth.gen_x(w)
     scales = synth.gen_scales(w, kind)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     compare_layout(g.views_numpy(), olay)
     if kind == 0:
         od, os_ = oracle.dispatch(olay, x, q)
@@ -95,7 +95,7 @@ def test_zero_rows_and_groups():
     xf[3] = np.random.default_rng(0).standard_normal(256) * 1e4
     x = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(2, 6, 256)
     olay = oracle.layout(2, 6, 4, 2, 1, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     for q in FP8T + FP8G:
         od, os_ = oracle.dispatch(olay, x, q)
         data, sc = g.lay.alloc_recv(q, olay.rows)
@@ -134,7 +134,7 @@ def test_full_size_sampled(q, kind):
     rng = np.random.default_rng(q)
     topk = synth.gen_topk(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     x_dev = synth.gen_x_device(w)
     x = bf16_bits(x_dev).reshape(w.N, w.H)
     scales = synth.gen_scales(w, kind)

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import GpuRun, bf16_bits, compare_layout, to_dev_bf16
+from gpu_harness import GpuPath, bf16_bits, compare_layout, to_dev_bf16
 from test_gpu_parity import check_combine, check_dispatch
 
 pytestmark = pytest.mark.gpu
@@ -50,7 +50,7 @@ def test_random_config(seed):
     x = synth.gen_x(w)
     shared = synth.gen_shared(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     assert g.rows == olay.rows
     compare_layout(g.views_numpy(), olay)
     x_dev = to_dev_bf16(x) if w.N else torch.empty((0, w.H), dtype=torch.bfloat16, device="cuda")

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import GpuRun, bf16_bits, oracle_combine_sampled, to_dev_bf16
+from gpu_harness import GpuPath, bf16_bits, oracle_combine_sampled, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ def run_norm(w, quant=0, mark=4, check_composition=True):
     res = synth.gen_residual(w)
     gam = synth.gen_gamma(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     x_dev = to_dev_bf16(x)
     data, scales = g.dispatch(x_dev, quant)
     y = g.expert(quant, data, scales, mark)
@@ -79,7 +79,7 @@ def test_edges():
     run_norm(w)
     # no tokens at all: nothing to do
     w0 = synth.WORKLOADS[1].with_(T=0, H=256)
-    g = GpuRun(w0, np.zeros((w0.R, 0, w0.K), np.int64))
+    g = GpuPath(w0, np.zeros((w0.R, 0, w0.K), np.int64))
     e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
     g.lay.combine_add_rms_norm(e, torch.empty((0, w0.K), device="cuda"), e, torch.ones(256, dtype=torch.bfloat16,
                                device="cuda"), e)
@@ -87,7 +87,7 @@ def test_edges():
     # expert outputs shorter than the layout: capacity error, nothing written
     w = synth.WORKLOADS[1].with_(H=256)
     topk = synth.gen_topk(w)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     y = torch.zeros((g.rows - 1, w.H), dtype=torch.bfloat16, device="cuda")
     out = torch.full((w.N, w.H), 3.0, dtype=torch.bfloat16, device="cuda")
     res = torch.zeros((w.N, w.H), dtype=torch.bfloat16, device="cuda")
@@ -103,7 +103,7 @@ def test_full_size_workload2_sampled():
     topk = synth.gen_topk(w)
     wts = synth.gen_weights(w, topk)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
-    g = GpuRun(w, topk)
+    g = GpuPath(w, topk)
     x_dev = synth.gen_x_device(w)
     x = bf16_bits(x_dev).reshape(w.N, w.H)
     data, _ = g.dispatch(x_dev, 0)
