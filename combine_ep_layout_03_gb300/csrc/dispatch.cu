@@ -60,11 +60,18 @@ __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
     f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xffff0000u);
 }
 
-// int8 code of one element: round half even of fl(x * s), clamped.
-__device__ __forceinline__ uint32_t q8(float x, float s) {
-    int q = __float2int_rn(__fmul_rn(x, s));
-    q = max(-127, min(127, q));
-    return (uint32_t)q & 0xffu;
+// int8 code of one element: round half even of fl(x * s), clamped to +-127
+// (the low byte of the returned int is the code).
+__device__ __forceinline__ int q8i(float x, float s) {
+    const int q = __float2int_rn(__fmul_rn(x, s));
+    return max(-127, min(127, q));
+}
+
+// Low bytes of four ints packed into one word (element 0 in the low byte).
+__device__ __forceinline__ uint32_t pack4_low_bytes(int q0, int q1, int q2, int q3) {
+    const uint32_t lo = __byte_perm((uint32_t)q0, (uint32_t)q1, 0x0040);
+    const uint32_t hi = __byte_perm((uint32_t)q2, (uint32_t)q3, 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
 }
 
 template <int Q>
@@ -173,11 +180,14 @@ __device__ __forceinline__ void apply_scales(float f[VPT][8], const float* sc, i
     }
 }
 
+// Bits of max |f[i]|: a non-negative float, so its bits order like the value
+// (the CTA and warp reductions take integer maxima of them).  fmaxf skips a NaN
+// element, as a running "if (a > amax)" maximum does.
 __device__ __forceinline__ uint32_t absmax_bits8(const float f[8]) {
-    uint32_t m = 0;
+    float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = max(m, __float_as_uint(fabsf(f[i])));  // monotone for |x| >= 0
-    return m;
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    return __float_as_uint(m);
 }
 
 // Codes of 8 scaled elements with dynamic scale s (per-token / per-group modes).
@@ -185,8 +195,8 @@ template <int Q>
 __device__ __forceinline__ void encode_dynamic(const float f[8], float s, bool nonzero, uint32_t out[2]) {
     if (!nonzero) { out[0] = out[1] = 0; return; }
     if constexpr (Q == M_INT8) {
-        out[0] = q8(f[0], s) | (q8(f[1], s) << 8) | (q8(f[2], s) << 16) | (q8(f[3], s) << 24);
-        out[1] = q8(f[4], s) | (q8(f[5], s) << 8) | (q8(f[6], s) << 16) | (q8(f[7], s) << 24);
+        out[0] = pack4_low_bytes(q8i(f[0], s), q8i(f[1], s), q8i(f[2], s), q8i(f[3], s));
+        out[1] = pack4_low_bytes(q8i(f[4], s), q8i(f[5], s), q8i(f[6], s), q8i(f[7], s));
     } else {
         constexpr int C = QTraits<Q>::fp8;
         out[0] = cvt_fp8x2<C>(__fmul_rn(f[0], s), __fmul_rn(f[1], s)) |
@@ -410,20 +420,22 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
-// expert.  Threads 0..K-1 find the K experts (bisection over expert_base);
-// each destination then takes one pass over its scale-row slice (per-token
-// modes add one CTA reduction of the row maximum; each destination has its
-// own reduction slot, so one barrier per destination suffices) and every
-// thread stores its codes directly.  The cost is dominated by reading K scale
-// rows of H floats per token from L2.
+// expert.  Warp 0 finds the experts of the valid destinations (bisection over
+// expert_base) and lists them compactly; each destination then takes one pass
+// over its scale-row slice (per-token modes add one CTA reduction of the row
+// maximum; each destination has its own reduction slot, so one barrier per
+// destination suffices) and every thread stores its codes directly.  The next
+// destination's scale slice is loaded into registers while the current one is
+// encoded, so its L2 latency overlaps the barrier and the stores.
 template <int Q, int VPT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024 / VPT)
 dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
     extern __shared__ int sbase[];   // [E+1] first row of each expert
     __shared__ int sdst[kMaxTopk];
     __shared__ int sexp[kMaxTopk];
-    __shared__ uint32_t sred[8][kMaxTopk];
+    __shared__ int snv;
+    __shared__ uint32_t sred[32][kMaxTopk];
     const int total = a.expert_base[a.E];
     if ((int64_t)total > a.cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
@@ -433,6 +445,20 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
     __syncthreads();
+    // this thread's scale slice of expert e: VPT x 2 float4
+    auto load_scales = [&](float4 (&sc)[VPT][2], int e) {
+        const float4* srow = reinterpret_cast<const float4*>(a.smooth + (int64_t)e * a.H);
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * NT + tid;
+            if (vi < a.nvec) {
+                sc[u][0] = __ldg(srow + 2 * vi);
+                sc[u][1] = __ldg(srow + 2 * vi + 1);
+            } else {
+                sc[u][0] = sc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
     const int64_t items = a.N + a.E;
     for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
         if (w >= a.N) {
@@ -442,9 +468,9 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
             zero_rows(a, r0, r1);
             continue;
         }
-        __syncthreads();   // sdst / sexp / sred of the previous token are consumed
-        if (tid < a.K) {
-            const int d = a.dst_row[w * a.K + tid];
+        __syncthreads();   // sdst / sexp / snv / sred of the previous token are consumed
+        if (warp == 0) {
+            const int d = lane < a.K ? a.dst_row[w * a.K + lane] : -1;
             int lo = 0;
             if (d >= 0) {
                 int hi = a.E;   // last expert e with sbase[e] <= d
@@ -453,45 +479,57 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                     if (sbase[mid] <= d) lo = mid; else hi = mid;
                 }
             }
-            sdst[tid] = d;
-            sexp[tid] = lo;
+            const unsigned valid = __ballot_sync(kFull, d >= 0);
+            if (d >= 0) {
+                const int j = __popc(valid & ((1u << lane) - 1u));
+                sdst[j] = d;
+                sexp[j] = lo;
+            }
+            if (lane == 0) snv = __popc(valid);
         }
         const uint16_t* xrow = a.x + w * a.H;
-        uint4 v[VPT];
+        float xf[VPT][8];   // the row as floats, unpacked once for all destinations
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
-            v[u] = vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0);
+            unpack8(vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), xf[u]);
         }
         __syncthreads();
-        for (int k = 0; k < a.K; ++k) {
-            const int d = sdst[k];
-            if (d < 0) continue;
+        const int nvd = snv;
+        float4 sc[VPT][2];
+        if (nvd > 0) load_scales(sc, sexp[0]);
+        for (int j = 0; j < nvd; ++j) {
+            const int d = sdst[j];
             float f[VPT][8];
 #pragma unroll
-            for (int u = 0; u < VPT; ++u) unpack8(v[u], f[u]);
-            apply_scales<VPT>(f, a.smooth + (int64_t)sexp[k] * a.H, EP_SCALES_PER_CHANNEL, NT, a.nvec);
+            for (int u = 0; u < VPT; ++u) {
+                f[u][0] = __fmul_rn(xf[u][0], sc[u][0].x); f[u][1] = __fmul_rn(xf[u][1], sc[u][0].y);
+                f[u][2] = __fmul_rn(xf[u][2], sc[u][0].z); f[u][3] = __fmul_rn(xf[u][3], sc[u][0].w);
+                f[u][4] = __fmul_rn(xf[u][4], sc[u][1].x); f[u][5] = __fmul_rn(xf[u][5], sc[u][1].y);
+                f[u][6] = __fmul_rn(xf[u][6], sc[u][1].z); f[u][7] = __fmul_rn(xf[u][7], sc[u][1].w);
+            }
+            if (j + 1 < nvd) load_scales(sc, sexp[j + 1]);   // overlaps the rest of this destination
             float s_tok = 0.0f, inv = 0.0f, amax = 0.0f;
             if constexpr (TR::token) {
                 uint32_t m = 0;
 #pragma unroll
                 for (int u = 0; u < VPT; ++u) m = max(m, absmax_bits8(f[u]));
                 for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
-                if (lane == 0) sred[warp][k] = m;
+                if (lane == 0) sred[warp][j] = m;
                 __syncthreads();
                 m = 0;
-                for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i][k]);
+                for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i][j]);
                 amax = __uint_as_float(m);
                 s_tok = __fdiv_rn(TR::dmax, amax);
                 inv = __fdiv_rn(1.0f, s_tok);
             }
             uint8_t* row = a.data + (int64_t)d * a.row_bytes;
-            uint8_t* srow = a.scales ? a.scales + (int64_t)d * a.scale_bytes : nullptr;
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
                 uint32_t packed[2], sb = 0;
                 float gi = 0.0f;
-                encode_vec<Q>(v[u], f[u], s_tok, amax > 0.0f, packed, sb, gi);
+                // the raw vector is only read by the MX modes, which take no input scales
+                encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
                 const int vi = u * NT + tid;
                 if (vi < a.nvec) {
                     st_v2(row + (int64_t)vi * 8, make_uint2(packed[0], packed[1]));
@@ -501,11 +539,15 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 }
             }
             if constexpr (TR::token) {
-                if (tid == 0) reinterpret_cast<float*>(srow)[0] = inv;
+                if (tid == 0) reinterpret_cast<float*>(a.scales + (int64_t)d * a.scale_bytes)[0] = inv;
             }
         }
     }
 }
+
+#ifndef EP_EXPERT_SCALED_VPT
+#define EP_EXPERT_SCALED_VPT 4   // 16-byte vectors per thread in the per-expert-scale kernel
+#endif
 
 #ifndef EP_DISPATCH_LAG
 #define EP_DISPATCH_LAG 4
@@ -738,16 +780,18 @@ cudaError_t launch_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st)
         if constexpr (QTraits<Q>::mx) {
             return cudaErrorInvalidValue;
         } else {
+            constexpr int EV = EP_EXPERT_SCALED_VPT;
+            const int ent = ((a.nvec + EV - 1) / EV + 31) / 32 * 32;
             const size_t smem = sizeof(int) * (size_t)(a.E + 1);
             int occ = 0;
             cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &occ, dispatch_expert_scaled_kernel<Q, VPT>, nt, smem);
+                &occ, dispatch_expert_scaled_kernel<Q, EV>, ent, smem);
             if (err != cudaSuccess) return err;
             const int64_t items = a.N + a.E;
             int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
             if (grid > items) grid = items;
             if (grid < 1) grid = 1;
-            dispatch_expert_scaled_kernel<Q, VPT><<<(unsigned)grid, nt, smem, st>>>(a);
+            dispatch_expert_scaled_kernel<Q, EV><<<(unsigned)grid, ent, smem, st>>>(a);
             return cudaGetLastError();
         }
     }
