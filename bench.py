@@ -234,7 +234,7 @@ def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt="", trows=0):
     N, H, K, S = w.N, w.H, w.K, w.num_shared
     disp = N * H * 2 + N * K * 4 + rows * (db + sb)
     if fmt == "pre":
-        disp = N * (db + sb) + N * K * 4 + rows * (db + sb) + (rows * 4 if sb else 0)
+        disp = N * (db + sb) + N * K * 4 + rows * (db + sb)
     norm = N * H * 2 * 3 + H * 2 + N * 4 if fmt == "norm" else 0   # residual in; x, rstd out
     if fmt == "split":
         # send: x in, arrival rows out; wait: V arrival rows in, grouped rows out
@@ -541,14 +541,15 @@ def launches_per_step(quant, recv_layout, fmt):
     """Kernels of this library launched per step: layout 3 (count, scan,
     assign), dispatch 1, combine 1; the per-rank layout adds 2 (scan, assign);
     the two-phase form adds a wait kernel to each exchange; a scale gather
-    follows the dispatch for pre-encoded rows with scales and for block-major
-    MX / per-group scales."""
+    follows the dispatch for block-major MX / per-group scales (pre-encoded
+    row-major scale rows travel with the data rows, as the bench's are
+    16-byte rows from 16-byte aligned buffers)."""
     n = 5
     if recv_layout == "rank" or fmt == "split":
         n += 2
     if fmt == "split":
         n += 2
-    if (fmt == "pre" and quant not in (0, 1)) or (fmt == "bm" and quant in (4, 5, 6, 9, 10)):
+    if fmt == "bm" and quant in (4, 5, 6, 9, 10):
         n += 1
     return n
 

@@ -664,7 +664,7 @@ cudaError_t launch_scale_gather(const ep_handle* h, const DispatchArgs& a, const
 }
 
 __global__ void __launch_bounds__(128)
-dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
+dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes, int scale_tma) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
     int32_t* sdst = reinterpret_cast<int32_t*>(smem + (size_t)nstages * stage_bytes);
@@ -685,6 +685,7 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
         for (int e = blockIdx.x; e < a.E; e += gridDim.x) {
             const int64_t r0 = (int64_t)a.expert_base[e] + a.recv_cnt[e];
             zero_rows_part(a, r0, a.expert_base[e + 1], tid - 32, blockDim.x - 32);
+            if (scale_tma) zero_scale_rows(a, r0, a.expert_base[e + 1], tid - 32, blockDim.x - 32);
         }
         return;
     }
@@ -693,6 +694,7 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
     const int64_t G = gridDim.x;
     const int64_t cnt = a.N > (int64_t)blockIdx.x ? (a.N - 1 - blockIdx.x) / G + 1 : 0;
     const uint32_t row = (uint32_t)a.row_bytes;
+    const uint32_t srb = scale_tma ? (uint32_t)a.scale_bytes : 0u;   // scale row after the data row
     const uint8_t* dst_bytes = reinterpret_cast<const uint8_t*>(a.dst_row);
     auto issue = [&](int64_t j) {
         const int s = (int)(j % nstages);
@@ -701,9 +703,10 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
         const int64_t b0 = (first * 4) & ~(int64_t)15;
         const int64_t b1 = ((first + a.K) * 4 + 15) & ~(int64_t)15;
         const uint32_t wbytes = (uint32_t)(b1 - b0);
-        mbar_arrive_expect_tx(&full[s], row + wbytes);
+        mbar_arrive_expect_tx(&full[s], row + srb + wbytes);
         bulk_load(stages + (size_t)s * stage_bytes, reinterpret_cast<const uint8_t*>(a.x) + n * row, row,
                   &full[s]);
+        if (srb) bulk_load(stages + (size_t)s * stage_bytes + row, a.xs + n * srb, srb, &full[s]);
         bulk_load(sdst + s * kDstSlotInts, dst_bytes + b0, wbytes, &full[s]);
     };
     const int64_t pro = cnt < nstages ? cnt : nstages;
@@ -718,7 +721,10 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
         const uint8_t* src = stages + (size_t)s * stage_bytes;
         for (int k = 0; k < a.K; ++k) {
             const int r = d[k];
-            if (r >= 0) bulk_store(a.data + (int64_t)r * row, src, row);
+            if (r >= 0) {
+                bulk_store(a.data + (int64_t)r * row, src, row);
+                if (srb) bulk_store(a.scales + (int64_t)r * srb, src + row, srb);
+            }
         }
         bulk_commit();
         if (j >= kTmaLag) {
@@ -737,21 +743,33 @@ dispatch_bf16_tma_kernel(DispatchArgs a, int nstages, int stage_bytes) {
     }
 }
 
+// Pre-encoded row-major scale rows of whole 16-byte units travel with the data
+// rows through the bulk-copy ring (no gather pass).
+bool scale_rows_by_tma(const DispatchArgs& a) {
+    return a.xs && a.scale_bytes > 0 && !a.scales_t && a.scale_bytes % 16 == 0 &&
+           ((uintptr_t)a.xs % 16) == 0 && ((uintptr_t)a.scales % 16) == 0;
+}
+
 cudaError_t launch_bf16_tma(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
-    const int stage_bytes = (a.row_bytes + 127) / 128 * 128;
+    const int scale_tma = scale_rows_by_tma(a) ? 1 : 0;
+    const int stage_bytes = (a.row_bytes + (scale_tma ? a.scale_bytes : 0) + 127) / 128 * 128;
     const int per_stage = stage_bytes + kDstSlotInts * 4 + 8;
-    int nstages = kDispatchSmemBudget / EP_DISPATCH_CTAS_PER_SM / per_stage;
+    // up to EP_DISPATCH_CTAS_PER_SM issuing CTAs per SM, fewer when their share
+    // of the shared-memory budget would hold too few stages for the store lag
+    int ctas = EP_DISPATCH_CTAS_PER_SM;
+    while (ctas > 1 && kDispatchSmemBudget / ctas / per_stage < kTmaLag + 2) --ctas;
+    int nstages = kDispatchSmemBudget / ctas / per_stage;
     if (nstages > 32) nstages = 32;
     if (nstages < kTmaLag + 2) return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)nstages * per_stage;
     cudaError_t err = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    int64_t grid = (int64_t)h->num_sms * EP_DISPATCH_CTAS_PER_SM;
+    int64_t grid = (int64_t)h->num_sms * ctas;
     const int64_t items = a.N > a.E ? a.N : a.E;
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
-    dispatch_bf16_tma_kernel<<<(unsigned)grid, 128, smem, st>>>(a, nstages, stage_bytes);
+    dispatch_bf16_tma_kernel<<<(unsigned)grid, 128, smem, st>>>(a, nstages, stage_bytes, scale_tma);
     return cudaGetLastError();
 }
 
@@ -827,7 +845,8 @@ cudaError_t launch_dispatch_encode(const ep_handle* h, const DispatchArgs& a, in
 
 cudaError_t launch_dispatch_bytes(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     cudaError_t err = launch_bf16_tma(h, a, st);
-    if (err == cudaSuccess && a.scale_bytes && a.xs) err = launch_scale_gather(h, a, a.xs, st);
+    if (err == cudaSuccess && a.scale_bytes && a.xs && !scale_rows_by_tma(a))
+        err = launch_scale_gather(h, a, a.xs, st);
     return err;
 }
 

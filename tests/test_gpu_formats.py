@@ -101,6 +101,28 @@ def test_pre_encoded_scale_rows_not_16_byte_units(q, H, block_major):
     assert np.array_equal(scales.cpu().numpy(), os_)
 
 
+def test_pre_encoded_scale_source_not_16_byte_aligned():
+    # 16-byte scale rows whose source starts 4 bytes past a 16-byte boundary take
+    # the gather instead of the bulk copies; the result is the same
+    w = small(1, H=512, alpha=4, T=50)
+    q = ep.EP_QUANT_MXFP8_E4M3
+    topk = synth.gen_topk(w)
+    olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    lay, _, rows = expert_layout(w, topk)
+    db, sb = ep.ep_recv_row_bytes(w.H, q)
+    src_d, src_s = synth.gen_encoded_rows(w, db, sb)
+    buf = torch.zeros(src_s.size + 16, dtype=torch.uint8, device="cuda")
+    xs = buf[4:4 + src_s.size]
+    xs.copy_(torch.from_numpy(src_s.reshape(-1)))
+    assert xs.data_ptr() % 16 == 4
+    data, scales = lay.alloc_recv(q, rows)
+    scales.fill_(0x21)
+    lay.dispatch_ex(torch.from_numpy(src_d).cuda(), q, data, scales, x_scales=xs, pre_encoded=True)
+    assert lay.status() == ep.EP_OK
+    assert np.array_equal(data.cpu().numpy(), oracle.dispatch_bytes(olay, src_d))
+    assert np.array_equal(scales.cpu().numpy(), oracle.dispatch_bytes(olay, src_s))
+
+
 @pytest.mark.parametrize("q", [0, 4, 6, 9])
 def test_pre_encoded_per_rank_layout(q):
     w = small(1, H=512, alpha=1, T=100)
