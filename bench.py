@@ -481,38 +481,54 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
 
 # --------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, quant, topk, wts, x_bits, sh_bits, budget_s):
-    """The oracle as it stands, single-threaded: layout over the whole routing,
-    then dispatch (rows one by one through recv_src) and combine of the first n
-    source tokens, n chosen so the work takes about budget_s.  sh_bits holds the
-    shared rows of the leading ranks ([R', S, T, H]) or None.
-    Returns (tokens/s, description, seconds spent, n)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, quant, topk, wts, x_bits, sh_bits, budget_s, threads=1):
+    """The oracle as it stands: layout over the whole routing (one thread), then
+    dispatch (rows one by one through recv_src), the stand-in expert and combine
+    of the first n source tokens, n chosen so the work takes about budget_s.
+    With threads > 1 the n tokens are split into contiguous chunks run on that
+    many threads at once (the oracle's C calls release the interpreter lock and
+    share no state).  sh_bits holds the shared rows of the leading ranks
+    ([R', S, T, H]) or None.  Returns (tokens/s, description, seconds spent, n)."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     t0 = time.perf_counter()
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
     t_layout = time.perf_counter() - t0
     K = w.K
     n_max = w.N if sh_bits is None else sh_bits.shape[0] * w.T
 
-    def run(n):
-        tokens = np.arange(n)
+    def part(a, b):
+        tokens = np.arange(a, b)
         d = olay.dst_row.reshape(-1, K)[tokens].reshape(-1)
         rows = np.unique(d[d >= 0])
         ymap = np.full(max(olay.rows, 1), -1, np.int64)
         ymap[rows] = np.arange(len(rows))
-        a = time.perf_counter()
         data, scales = oracle.dispatch_rows(olay, x_bits, quant, rows)
-        b = time.perf_counter()
         if quant == 0:
             y = data.view(np.uint16).reshape(len(rows), w.H)
         else:
             y = oracle.expert_rows(olay, rows, w.H, quant, data, scales)
-        c = time.perf_counter()
-        oracle.combine(olay, y, wts, sh_bits, 0, n, ymap)
-        dd = time.perf_counter()
-        return (b - a) + (dd - c)
+        oracle.combine(olay, y, wts, sh_bits, a, b, ymap)
 
-    n = min(n_max, 8)
+    def run(n):
+        a = time.perf_counter()
+        if threads <= 1:
+            part(0, n)
+        else:
+            step = -(-n // threads)
+            chunks = [(c, min(n, c + step)) for c in range(0, n, step)]
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                list(ex.map(lambda c: part(*c), chunks))
+        return time.perf_counter() - a
+
+    n = min(n_max, 8 * max(1, threads))
     t = run(n)
     spent = t_layout + t
     while t < budget_s * 0.5 and n < n_max:
@@ -520,8 +536,9 @@ def oracle_sample(w, quant, topk, wts, x_bits, sh_bits, budget_s):
         t = run(n)
         spent += t
     per_token = t_layout / w.N + t / n
-    desc = (f"layout of all {w.N} tokens ({t_layout*1e3:.1f} ms) + dispatch and combine of the "
-            f"first {n} source tokens ({t:.2f} s), extrapolated per token")
+    desc = (f"layout of all {w.N} tokens ({t_layout*1e3:.1f} ms, 1 thread) + dispatch, stand-in expert and "
+            f"combine of the first {n} source tokens ({t:.2f} s, {threads} thread{'s' if threads > 1 else ''}),"
+            f" extrapolated per token")
     return 1.0 / per_token, desc, spent, n
 
 
@@ -607,8 +624,11 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xb = host_x_bits(res["x_dev"], w)
         sh0 = host_shared_lead(res["sh_dev"], w)
-        v, desc, spent, n = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget)
-        cpu = {"value": round(v, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        cores = host_cores()
+        v, desc, spent, n = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget, cores)
+        v1, _, _, _ = oracle_sample(w, quant, res["topk"], res["wts"], xb, sh0, args.cpu_budget / 2, 1)
+        cpu = {"value": round(v, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "single_thread_value": round(v1, 1),
                "sample": desc + SAMPLE_NOTE * bool(kind or mask_dims) + FORMAT_NOTE * bool(fmt)}
 
     e2e = None
@@ -656,8 +676,9 @@ def run_reference(args, w, quant, kind=0, mask_dims=0):
     sh = synth.gen_shared(w.with_(R=2)) if w.num_shared else None
     budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
     vals, descs = [], None
+    cores = host_cores()
     for i in range(args.warmup + args.steps):
-        v, desc, spent, n = oracle_sample(w, quant, topk, wts, x_bits, sh, budget)
+        v, desc, spent, n = oracle_sample(w, quant, topk, wts, x_bits, sh, budget, cores)
         if i >= args.warmup:
             vals.append(v)
             descs = desc
@@ -670,7 +691,7 @@ def run_reference(args, w, quant, kind=0, mask_dims=0):
         "dtype": "bf16" if quant == 0 else f"bf16->{QNAME[quant]}",
         "data": "synthetic (same seeded recipe as the GPU arm)", "impl": "reference",
         "config": workload_config(w, quant, args.workload, kind, mask_dims),
-        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
                          "kind": "oracle", "sample": descs + SAMPLE_NOTE * bool(kind or mask_dims)},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
