@@ -75,6 +75,6 @@ def test_reference_arm_line_small_workload(monkeypatch, capsys):
     assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1", "--workload", "1"]) == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_cores()
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["metric"] == bench.METRIC
