@@ -170,7 +170,11 @@ ep_status ep_recv_row_bytes(int32_t hidden, ep_quant_mode quant,
  * ep_layout_workspace_size() bytes, 256-byte aligned.  The small host-side
  * struct is allocated with malloc; free it with ep_handle_destroy.  The
  * workspace must outlive the handle.  A handle can be reused for many
- * ep_layout calls with the same params. */
+ * ep_layout calls with the same params.  All calls on one handle share its
+ * workspace (the layout arrays, the status word, the per-token scale staging
+ * rows of block-major dispatch): issue them on one stream, or order them
+ * across streams with events; separate handles are independent.  The host
+ * struct is not locked: use one handle from one host thread at a time. */
 ep_status ep_handle_create(const ep_params* params, void* workspace,
                            size_t workspace_bytes, ep_handle** out);
 
