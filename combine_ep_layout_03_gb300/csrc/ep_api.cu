@@ -643,6 +643,46 @@ ep_status ep_combine_add_rms_norm(const ep_handle* hc, const void* y, int64_t y_
     return from_cuda(launch_combine_norm(h, a, (cudaStream_t)stream));
 }
 
+ep_status ep_step_host(ep_handle* h, ep_quant_mode q, const int64_t* topk_host, const float* w_host,
+                       const void* x_host, const void* shared_host, int32_t S, void* out_host,
+                       const ep_step_buffers* dev, ep_stream_t stream) {
+    if (!h || !dev) return EP_ERR_INVALID_ARG;
+    if (!valid_quant(q)) return EP_ERR_UNSUPPORTED;
+    if (S < 0 || S > kMaxShared) return EP_ERR_INVALID_ARG;
+    if (!dev->y && q != EP_QUANT_NONE) return EP_ERR_INVALID_ARG;   // identity rows need bf16
+    const int64_t N = h->N, K = h->K, H = h->H;
+    if (N > 0) {
+        if (!topk_host || !w_host || !x_host || !out_host) return EP_ERR_INVALID_ARG;
+        if (S > 0 && (!shared_host || !dev->shared)) return EP_ERR_INVALID_ARG;
+        if (!dev->topk || !dev->weights || !dev->x || !dev->out) return EP_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    if (N > 0) {
+        cudaError_t e = cudaMemcpyAsync(dev->topk, topk_host, sizeof(int64_t) * (size_t)(N * K),
+                                        cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dev->weights, w_host, sizeof(float) * (size_t)(N * K), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dev->x, x_host, 2 * (size_t)(N * H), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && S > 0)
+            e = cudaMemcpyAsync(dev->shared, shared_host, 2 * (size_t)(N * H) * (size_t)S, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return EP_ERR_CUDA;
+    }
+    ep_status s = ep_layout(h, dev->topk, stream);
+    if (s == EP_OK)
+        s = ep_dispatch(h, dev->x, q, dev->recv_data, dev->recv_scales, dev->recv_rows_capacity, stream);
+    if (s != EP_OK) return s;
+    if (dev->y) {
+        s = ep_combine(h, dev->y, dev->y_rows_capacity, dev->weights, dev->shared, S, dev->out, stream);
+    } else {   // identity experts: the bf16 receive rows are the expert outputs
+        s = ep_combine(h, dev->recv_data, dev->recv_rows_capacity, dev->weights, dev->shared, S, dev->out, stream);
+    }
+    if (s != EP_OK) return s;
+    if (N > 0 && cudaMemcpyAsync(out_host, dev->out, 2 * (size_t)(N * H), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return EP_ERR_CUDA;
+    return EP_OK;
+}
+
 ep_status ep_test_combine_stalled(const ep_handle* hc, const void* y, int64_t y_cap, const float* w,
                                   void* out, uint32_t max_polls, ep_stream_t stream) {
     ep_handle* h = const_cast<ep_handle*>(hc);

@@ -60,6 +60,13 @@ class ep_layout_views(ctypes.Structure):
         ("rank_tok_base", ctypes.c_void_p), ("tok_capacity", ctypes.c_int64)]
 
 
+class ep_step_buffers(ctypes.Structure):
+    _fields_ = [("topk", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("shared", ctypes.c_void_p), ("out", ctypes.c_void_p), ("recv_data", ctypes.c_void_p),
+                ("recv_scales", ctypes.c_void_p), ("recv_rows_capacity", ctypes.c_int64),
+                ("y", ctypes.c_void_p), ("y_rows_capacity", ctypes.c_int64)]
+
+
 class ep_layout_outputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "status", "cnt", "is_token_in_rank", "num_tokens_per_rank", "recv_cnt", "aligned_cnt",
@@ -100,6 +107,7 @@ def _load():
         "ep_dispatch_ex": ([vp, vp, vp, st, vp, st, ctypes.c_uint32, vp, vp, i64, vp], st),
         "ep_combine_add_rms_norm": ([vp, vp, i64, vp, vp, i32, vp, vp, ctypes.c_float, vp, vp, vp, vp], st),
         "ep_test_combine_stalled": ([vp, vp, i64, vp, vp, ctypes.c_uint32, vp], st),
+        "ep_step_host": ([vp, st, vp, vp, vp, vp, i32, vp, ctypes.POINTER(ep_step_buffers), vp], st),
         "ep_dispatch_async": ([vp, vp, st, vp, st, vp, vp, i64, vp], st),
         "ep_dispatch_wait": ([vp, st, vp, vp, i64, ctypes.c_uint32, vp, vp, i64, vp], st),
         "ep_combine_async": ([vp, vp, i64, vp, i64, vp], st),
@@ -232,6 +240,24 @@ def ep_combine_add_rms_norm(h: int, y, y_rows_capacity: int, topk_weights, share
                                         int(num_shared), _ptr(residual), _ptr(gamma), float(eps),
                                         _ptr(norm_out), _ptr(x_out), _ptr(rstd_out), _stream(stream)),
            "ep_combine_add_rms_norm")
+
+
+def step_buffers(topk, weights, x, out, recv_data, recv_scales=None, shared=None, y=None,
+                 H: int | None = None) -> ep_step_buffers:
+    """ep_step_buffers from device tensors (capacities from their sizes)."""
+    b = ep_step_buffers()
+    b.topk, b.weights, b.x, b.out = _ptr(topk), _ptr(weights), _ptr(x), _ptr(out)
+    b.shared, b.recv_data, b.recv_scales, b.y = _ptr(shared), _ptr(recv_data), _ptr(recv_scales), _ptr(y)
+    b.recv_rows_capacity = recv_data.shape[0]
+    b.y_rows_capacity = 0 if y is None else y.numel() // (H or y.shape[-1])
+    return b
+
+
+def ep_step_host(h: int, quant: int, topk_host, weights_host, x_host, shared_host, num_shared: int, out_host,
+                 bufs: ep_step_buffers, stream=None) -> None:
+    """One step from (pinned) host tensors: copy in, layout, dispatch, combine, copy out."""
+    _check(_lib.ep_step_host(h, quant, _ptr(topk_host), _ptr(weights_host), _ptr(x_host), _ptr(shared_host),
+                             int(num_shared), _ptr(out_host), ctypes.byref(bufs), _stream(stream)), "ep_step_host")
 
 
 def ep_test_combine_stalled(h: int, y, y_rows_capacity: int, topk_weights, out, max_polls: int,

@@ -450,6 +450,44 @@ ep_status ep_combine_add_rms_norm(const ep_handle* handle, const void* y, int64_
                                   const void* residual, const void* gamma, float eps, void* norm_out,
                                   void* x_out, float* rstd_out, ep_stream_t stream);
 
+/* ---- One step from host buffers ------------------------------------------- */
+
+/* Device buffers one ep_step_host call works in (all caller-owned device
+ * memory; the call allocates nothing).  topk [R,T,K] int64, weights [R,T,K]
+ * float32, x [R*T, H] bf16 (or, for quant != NONE, the bf16 input that is
+ * quantised), shared [R, num_shared, T, H] bf16 (NULL when num_shared = 0),
+ * out [R*T, H] bf16; recv_data / recv_scales as for ep_dispatch with
+ * recv_rows_capacity rows; y [y_rows_capacity, H] bf16 holds the expert
+ * outputs the combine reads, or NULL for quant NONE, where the combine reads
+ * the receive rows themselves (identity experts). */
+typedef struct ep_step_buffers {
+    int64_t* topk;
+    float* weights;
+    void* x;
+    void* shared;
+    void* out;
+    void* recv_data;
+    void* recv_scales;
+    int64_t recv_rows_capacity;
+    const void* y;
+    int64_t y_rows_capacity;
+} ep_step_buffers;
+
+/* Device + host.  One whole step from host buffers, enqueued on the stream:
+ * copies topk_host, weights_host, x_host (and shared_host when num_shared >
+ * 0) into the device buffers, runs ep_layout, ep_dispatch (quant) and
+ * ep_combine (out = weighted sum of y, or of the receive rows when y is NULL),
+ * and copies out to out_host.  Host buffers should be pinned (page-locked) so
+ * the copies run asynchronously and overlap work on other streams; two steps
+ * on two streams with separate ep_step_buffers and handles overlap one step's
+ * copies with the other's kernels.  Returns once everything is enqueued; the
+ * host buffers must stay valid until the stream reaches the end of the step.
+ * Errors as for the calls it makes. */
+ep_status ep_step_host(ep_handle* handle, ep_quant_mode quant, const int64_t* topk_host,
+                       const float* weights_host, const void* x_host, const void* shared_host,
+                       int32_t num_shared, void* out_host, const ep_step_buffers* dev,
+                       ep_stream_t stream);
+
 /* ---- Test hook ------------------------------------------------------------ */
 
 /* Device.  For tests of the bounded waits only, never part of the path: runs

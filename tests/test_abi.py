@@ -292,3 +292,21 @@ def test_stalled_combine_hook_validation():
     assert L.ep_test_combine_stalled(h, A, 10, B, C, (1 << 22) + 1, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_test_combine_stalled(h, A, 10, None, C, 16, None) == ep.EP_ERR_INVALID_ARG
     ep.ep_handle_destroy(h)
+
+
+def test_step_host_validation():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    st, h, _ = _create_fake(p)
+    L = ep.lib
+    A, B, C, D = 1 << 40, 1 << 41, 1 << 42, 1 << 43
+    bufs = ep.ep_step_buffers()
+    bufs.topk, bufs.weights, bufs.x, bufs.out, bufs.recv_data = A, B, C, D, A
+    bufs.recv_rows_capacity = 64
+    ref = ctypes.byref(bufs)
+    assert L.ep_step_host(h, 0, A, B, C, None, 0, D, None, None) == ep.EP_ERR_INVALID_ARG      # no buffers
+    assert L.ep_step_host(h, 4, A, B, C, None, 0, D, ref, None) == ep.EP_ERR_INVALID_ARG       # quantised, no y
+    assert L.ep_step_host(h, 0, A, B, C, None, 17, D, ref, None) == ep.EP_ERR_INVALID_ARG      # too many shared
+    assert L.ep_step_host(h, 0, A, B, C, None, 2, D, ref, None) == ep.EP_ERR_INVALID_ARG       # shared missing
+    assert L.ep_step_host(h, 0, None, B, C, None, 0, D, ref, None) == ep.EP_ERR_INVALID_ARG    # no host topk
+    assert L.ep_step_host(h, 11, A, B, C, None, 0, D, ref, None) == ep.EP_ERR_UNSUPPORTED
+    ep.ep_handle_destroy(h)
