@@ -107,12 +107,20 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_text(src: str) -> str:
+    """Source text without comments and blank space, so that a digest follows
+    the code only (a comment edit leaves a profile valid)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def source_digest(name: str) -> str:
     p = os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", name)
     h = hashlib.sha256()
     for f in (p, os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", "ep_internal.cuh")):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -3,7 +3,8 @@
 // sum"; MAX EPBatchManager.ep_combine: weighted sum of routed expert outputs,
 // plus the fused shared-expert outputs), rounded once to bf16.
 //
-// Persistent grid, one CTA per SM, tokens round-robin over CTAs.  Warp 0 is a
+// Persistent grid, two CTAs per SM (one with the RMSNorm epilogue), tokens
+// round-robin over CTAs.  Warp 0 is a
 // producer: per token it compacts the valid slots (ballot, slot order kept),
 // and per chunk of the row it bulk-loads (cp.async.bulk, TMA) the chunk of each
 // valid expert row and of each shared row into a shared-memory stage, tracked
@@ -12,8 +13,8 @@
 // then release the stage on its "empty" mbarrier.  No register staging, so
 // the bytes in flight are bounded only by the stage ring.
 //
-// The stand-in expert (ep_expert_identity) is also here: it dequantises
-// receive rows back to bf16 for tests and benchmarks.
+// The stand-in experts (ep_expert_identity and its per-rank form) are also
+// here: they dequantise receive rows back to bf16 for tests and benchmarks.
 #include "ep_internal.cuh"
 #include "tma.cuh"
 

@@ -1,8 +1,10 @@
 // dispatch.cu -- permute-scatter of token rows into the receive layout, with
 // the encodings of CANN aclnnMoeDistributeDispatchV2's Formula section:
 //   quantMode 0  bf16 copy;
-//   quantMode 2  per-token dynamic int8: s = 127 / max|x|, code = rn(x * s),
-//                scale word 1/s;
+//   quantMode 1  static int8: code = rn(x * scales) saturated to [-128, 127];
+//   quantMode 2  per-token dynamic int8 / FP8: s = dstTypeMax / max|x * scales|,
+//                code = cast(x * scales * s), scale word 1/s;
+//   quantMode 3  the same per group of 128 elements (FP8), one 1/s per group;
 //   quantMode 4  MX: per 32-element block sharedExp = floor(log2(max|x|)) - emax,
 //                code = cast(x / 2^sharedExp) (e4m3 / e5m2, and e2m1 packed x2),
 //                e8m0 scale byte sharedExp + 127.
@@ -16,8 +18,8 @@
 // one expert each.  The four lanes 4m..4m+3 hold one 32-element MX block at
 // the same u.
 //
-// bf16 rows (quantMode 0) take a register-free path instead: one thread per
-// CTA drives the bulk-copy (TMA) engine.  A ring of shared-memory stages holds
+// bf16 rows (quantMode 0) take a register-free path instead: one thread in
+// each of two CTAs per SM drives the bulk-copy (TMA) engine.  A ring of shared-memory stages holds
 // a source row plus the 16-byte-aligned window of its dst_row entries, both
 // loaded by cp.async.bulk onto the stage's mbarrier; the row is then written
 // to its K destination rows by cp.async.bulk stores, one bulk group per token,
@@ -25,8 +27,9 @@
 // issued kTmaLag tokens earlier have read it.  Warps 1..3 of the CTA zero the
 // padding rows meanwhile.  The same kernel moves pre-encoded rows (DeepEP
 // "Normal Mode API", Quantization: x given as a (data, scale) tuple): the
-// source row is then any fixed number of bytes, and warps 1..3 also gather the
-// scale rows per receive row.
+// source row is then any fixed number of bytes, and a row-major scale row of
+// whole 16-byte units rides in the stage after it (other scale layouts are
+// filled by a gather pass per receive row).
 //
 // Scales can be written block-major (Modular MAX "EPBatchManager",
 // ep_dispatch output_scales of shape (hidden // block_size, max_recv_tokens)):
