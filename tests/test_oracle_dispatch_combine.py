@@ -223,3 +223,39 @@ def test_sampled_combine_matches_full_oracle(idx, q):
         sh_tok = shared.transpose(0, 2, 1, 3).reshape(w.N, w.num_shared, w.H)[tokens]
     o, ref, mag = oracle_combine_sampled(lay, x.reshape(w.N, w.H), wts, sh_tok, q, 8, tokens)
     assert np.array_equal(o, full[tokens])
+
+
+@pytest.mark.parametrize("q", [oracle.Q_INT8_STATIC, oracle.Q_E5M2, oracle.Q_FP8T_E4M3, oracle.Q_FP8T_E5M2,
+                               oracle.Q_FP8G_E4M3, oracle.Q_FP8G_E5M2])
+def test_expert_dequant_rows_more_modes(q):
+    # the stand-in expert's decode for the further modes, with torch's float8 decode as
+    # the independent route: code value (x the row's or group's 1/s), then bf16
+    import torch
+    w = small(4, 8)
+    topk = synth.gen_topk(w)
+    x = synth.gen_x(w)
+    lay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    rows = np.flatnonzero(lay.recv_src >= 0)[:16]
+    if q == oracle.Q_INT8_STATIC:
+        sc = synth.gen_scales(w, 2)
+        data, scales = oracle.dispatch_scaled(lay, x, q, topk, sc, 2)
+        data, scales = data[rows], scales[rows]
+    else:
+        data, scales = oracle.dispatch_rows(lay, x, q, rows)
+    y = f64(oracle.expert_rows(lay, rows, w.H, q, data, scales))
+    e5 = q in (oracle.Q_E5M2, oracle.Q_FP8T_E5M2, oracle.Q_FP8G_E5M2)
+    dt = torch.float8_e5m2 if e5 else torch.float8_e4m3fn
+    for i in range(len(rows)):
+        if q == oracle.Q_INT8_STATIC:
+            v = data[i].view(np.int8).astype(np.float32)
+        else:
+            codes = torch.from_numpy(data[i].copy()).view(dt).to(torch.float32).numpy()
+            if q == oracle.Q_E5M2:
+                mul = np.repeat(np.ldexp(1.0, scales[i].astype(np.int64) - 127), 32).astype(np.float32)
+            elif q in (oracle.Q_FP8T_E4M3, oracle.Q_FP8T_E5M2):
+                mul = np.full(w.H, scales[i].view(np.float32)[0], np.float32)
+            else:
+                mul = np.repeat(scales[i].view(np.float32), 128)
+            v = (codes * mul).astype(np.float32)
+        want = f64(oracle.bf16_from_f32(v))
+        assert np.array_equal(y[i], want)

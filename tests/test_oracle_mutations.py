@@ -70,6 +70,10 @@ MUTANTS = {
         "memcpy(out + (d - row_begin) * row_bytes, src + d * row_bytes, (size_t)row_bytes);"),
     "bytes_first_slot_only": ("        for (int k = 0; k < K; ++k) {\n            int64_t d = dst_row[n * K + k];\n            if (d < row_begin || d >= row_end) continue;\n            memcpy(out + (d - row_begin) * row_bytes, src + n",
                               "        for (int k = 0; k < 1; ++k) {\n            int64_t d = dst_row[n * K + k];\n            if (d < row_begin || d >= row_end) continue;\n            memcpy(out + (d - row_begin) * row_bytes, src + n"),
+    "expert_group_scale_index": ("memcpy(&inv, s + ((q == Q_FP8G_E4M3 || q == Q_FP8G_E5M2) ? 4 * (h / GROUP) : 0), 4);",
+                                 "memcpy(&inv, s + ((q == Q_FP8G_E4M3 || q == Q_FP8G_E5M2) ? 4 * (h / 32) : 0), 4);"),
+    "expert_static_codes_unsigned": ("                v = (float)(int8_t)d[h];\n            } else {",
+                                     "                v = (float)d[h];\n            } else {"),
     "rms_residual_dropped": ("double v = c[n * H + h] + (double)oracle_bf16_to_f32(residual[n * H + h]);",
                              "double v = c[n * H + h];"),
     "rms_eps_outside_sqrt": ("double r = 1.0 / sqrt(ss / (double)H + eps);",
@@ -110,6 +114,8 @@ def pins():
     cases += [lambda: ttl.test_combine_through_rank_expert_stage_closed_form(2, 24, 4),
               ttl.test_reduced_weights_equal_original_for_valid_entries]
     cases += [lambda s=s: tfm.test_dispatch_bytes_brute_force(s) for s in range(4)]
+    cases += [lambda: tdc.test_expert_dequant_rows_more_modes(oracle.Q_FP8G_E4M3),
+              lambda: tdc.test_expert_dequant_rows_more_modes(oracle.Q_INT8_STATIC)]
     cases += [trn.test_hand_worked_row, lambda: trn.test_constant_row(1e-3, 1e-6),
               lambda: trn.test_constant_row(0.75, 1e-6), lambda: trn.test_matches_torch_rms_norm_float64(1e-6)]
     return cases
