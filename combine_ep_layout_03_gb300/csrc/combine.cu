@@ -76,6 +76,12 @@ constexpr int kMetaInts = 32;   // per stage: [0] = valid slots, [1..16] = weigh
 #ifndef EP_COMBINE_STAGE_TARGET
 #define EP_COMBINE_STAGE_TARGET 49152
 #endif
+#ifndef EP_COMBINE_STAGE_TARGET_RANK
+#define EP_COMBINE_STAGE_TARGET_RANK 32768
+#endif
+#ifndef EP_COMBINE_CTAS_PER_SM_RANK
+#define EP_COMBINE_CTAS_PER_SM_RANK 3
+#endif
 #ifndef EP_COMBINE_GROUPS
 #define EP_COMBINE_GROUPS 1
 #endif
@@ -449,7 +455,11 @@ cudaError_t launch_combine_impl(const ep_handle* h, const CombineArgs& a, cudaSt
     if (a.N == 0) return cudaSuccess;
     CombineTma c;
     c.rows = a.K + a.S + (NORM ? 1 : 0);
-    const int ctas_per_sm = NORM ? 1 : EP_COMBINE_CTAS_PER_SM;
+    // the per-rank layout's combine (unit weights) runs three CTAs per SM with
+    // ~32 KB stages: its tokens fill two thirds of their K row slots on
+    // average, and more, smaller pipelines per SM keep more bytes in flight
+    const bool per_rank = (a.w == nullptr) && !a.slot_rows;
+    const int ctas_per_sm = NORM ? 1 : (per_rank ? EP_COMBINE_CTAS_PER_SM_RANK : EP_COMBINE_CTAS_PER_SM);
     const int budget = kCombineSmemBudget / ctas_per_sm;
     // NORM: two reduction barriers, two 32-slot partial-sum arrays, the x row
     // (float32) and gamma (bf16)
@@ -457,7 +467,7 @@ cudaError_t launch_combine_impl(const ep_handle* h, const CombineArgs& a, cudaSt
     // about EP_COMBINE_STAGE_TARGET bytes of row chunks per stage (with the x
     // row buffer, small enough for three stages), chunks of equal size
     // (multiples of 8 elements)
-    int target = EP_COMBINE_STAGE_TARGET;
+    int target = per_rank ? EP_COMBINE_STAGE_TARGET_RANK : EP_COMBINE_STAGE_TARGET;
     if (NORM) target = (budget - norm_bytes) / 3;
     int ch = (target / 2 / c.rows) & ~7;
     if (ch < 8) ch = 8;
