@@ -177,7 +177,10 @@ static float round_half_even(float v) {
 /*   quantOut = CastToInt8(xFp32 * dynamicScales)  (round half even)         */
 /*   sent scale = 1.0 / dynamicScales                                        */
 /* An all-zero row has dynamicScales = +inf; its codes are 0 and its sent    */
-/* scale is 1/inf = 0.                                                       */
+/* scale is 1/inf = 0.  Non-finite input follows IEEE arithmetic: the        */
+/* maximum skips NaN elements (a running greater-than maximum), an infinite  */
+/* element gives dynamicScales 0, a row of subnormals overflows 127/amax to  */
+/* +inf (codes +-127 from +-inf products), and a NaN product converts to 0.  */
 /* ------------------------------------------------------------------------ */
 /* The scaled input of quantModes 1-3: xFp32 = CastToFp32(X) x scales, one
  * factor per element (smooth == NULL: no scales, factor 1, no multiply). */
@@ -199,6 +202,7 @@ void oracle_quant_int8_row_scaled(int H, const uint16_t* x, const float* smooth,
         float r = 0.0f;
         if (amax > 0.0f) {
             r = round_half_even(scaled_x(x, smooth, h) * s);
+            if (r != r) r = 0.0f;   /* NaN product (0 x inf, inf x 0, a NaN input): code 0 */
             if (r > 127.0f) r = 127.0f;
             if (r < -127.0f) r = -127.0f;
         }
@@ -288,6 +292,7 @@ void oracle_quant_fp8_group_row(int H, int fp8, const uint16_t* x, const float* 
 void oracle_quant_int8_static_row(int H, const uint16_t* x, const float* smooth, int8_t* q) {
     for (int h = 0; h < H; ++h) {
         float r = round_half_even(scaled_x(x, smooth, h));
+        if (r != r) r = 0.0f;   /* NaN input or product: code 0 */
         if (r > 127.0f) r = 127.0f;
         if (r < -128.0f) r = -128.0f;
         q[h] = (int8_t)(int)r;
