@@ -421,6 +421,10 @@ dispatch_kernel(DispatchArgs a, int stage_bytes, int scale_off, int scale_bulk) 
     }
 }
 
+#ifndef EP_EXPERT_SCALED_VPT
+#define EP_EXPERT_SCALED_VPT 4   // 16-byte vectors per thread in the per-expert-scale kernel
+#endif
+
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
 // expert.  Warp 0 finds the experts of the valid destinations (bisection over
@@ -438,7 +442,9 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
     __shared__ int sdst[kMaxTopk];
     __shared__ int sexp[kMaxTopk];
     __shared__ int snv;
-    __shared__ uint32_t sred[32][kMaxTopk];
+    // per-destination warp maxima, [destination][warp]; the slots of absent
+    // warps stay 0 so that a destination's slots are read four at a time
+    __shared__ __align__(16) uint32_t sred[kMaxTopk][32];
     const int total = a.expert_base[a.E];
     if ((int64_t)total > a.cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
@@ -446,7 +452,9 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
     }
     const int NT = blockDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw4 = ((NT >> 5) + 3) >> 2;   // 16-byte groups of warp slots
     for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
+    for (int i = tid; i < kMaxTopk * 32; i += NT) (&sred[0][0])[i] = 0u;
     __syncthreads();
     // this thread's scale slice of expert e: VPT x 2 float4
     auto load_scales = [&](float4 (&sc)[VPT][2], int e) {
@@ -512,27 +520,60 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 f[u][6] = __fmul_rn(xf[u][6], sc[u][1].z); f[u][7] = __fmul_rn(xf[u][7], sc[u][1].w);
             }
             if (j + 1 < nvd) load_scales(sc, sexp[j + 1]);   // overlaps the rest of this destination
-            float s_tok = 0.0f, inv = 0.0f, amax = 0.0f;
+            float s_tok = 0.0f, amax = 0.0f;
             if constexpr (TR::token) {
-                uint32_t m = 0;
+                // row maximum: a tree over the thread's elements, one warp
+                // reduction instruction, then the warps' slots
+                float t[VPT];
 #pragma unroll
-                for (int u = 0; u < VPT; ++u) m = max(m, absmax_bits8(f[u]));
-                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
-                if (lane == 0) sred[warp][j] = m;
+                for (int u = 0; u < VPT; ++u) {
+                    const float a01 = fmaxf(fabsf(f[u][0]), fabsf(f[u][1]));
+                    const float a23 = fmaxf(fabsf(f[u][2]), fabsf(f[u][3]));
+                    const float a45 = fmaxf(fabsf(f[u][4]), fabsf(f[u][5]));
+                    const float a67 = fmaxf(fabsf(f[u][6]), fabsf(f[u][7]));
+                    t[u] = fmaxf(fmaxf(a01, a23), fmaxf(a45, a67));
+                }
+#pragma unroll
+                for (int w2 = 1; w2 < VPT; w2 <<= 1)
+#pragma unroll
+                    for (int u = 0; u + w2 < VPT; u += 2 * w2) t[u] = fmaxf(t[u], t[u + w2]);
+                // fmaxf returns the other operand for one NaN and NaN for two:
+                // the 0 operand makes an all-NaN slice 0, like a running maximum
+                uint32_t m = __float_as_uint(fmaxf(0.0f, t[0]));
+                m = __reduce_max_sync(kFull, m);
+                if (lane == 0) sred[j][warp] = m;
                 __syncthreads();
+                const uint4* slots = reinterpret_cast<const uint4*>(&sred[j][0]);
                 m = 0;
-                for (int i = 0; i < (NT >> 5); ++i) m = max(m, sred[i][j]);
+                for (int i = 0; i < nw4; ++i) {
+                    const uint4 q4 = slots[i];
+                    m = max(m, max(max(q4.x, q4.y), max(q4.z, q4.w)));
+                }
                 amax = __uint_as_float(m);
                 s_tok = __fdiv_rn(TR::dmax, amax);
-                inv = __fdiv_rn(1.0f, s_tok);
             }
+            // int8 with a finite scale: |fl(f * s)| <= 127 (1 + 2^-24) for every
+            // element, so the rounded code is within +-127 and the clamp is
+            // idle; a NaN product converts to 0.  Only an infinite scale (a
+            // row whose maximum is subnormal, or zero) needs the clamped form.
+            const bool no_clamp = (Q == M_INT8) && amax > 0.0f && !isinf(s_tok);
             uint8_t* row = a.data + (int64_t)d * a.row_bytes;
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
                 uint32_t packed[2], sb = 0;
                 float gi = 0.0f;
-                // the raw vector is only read by the MX modes, which take no input scales
-                encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
+                if (no_clamp) {
+                    const float* g = f[u];
+                    packed[0] = pack4_low_bytes(
+                        __float2int_rn(__fmul_rn(g[0], s_tok)), __float2int_rn(__fmul_rn(g[1], s_tok)),
+                        __float2int_rn(__fmul_rn(g[2], s_tok)), __float2int_rn(__fmul_rn(g[3], s_tok)));
+                    packed[1] = pack4_low_bytes(
+                        __float2int_rn(__fmul_rn(g[4], s_tok)), __float2int_rn(__fmul_rn(g[5], s_tok)),
+                        __float2int_rn(__fmul_rn(g[6], s_tok)), __float2int_rn(__fmul_rn(g[7], s_tok)));
+                } else {
+                    // the raw vector is only read by the MX modes, which take no input scales
+                    encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
+                }
                 const int vi = u * NT + tid;
                 if (vi < a.nvec) {
                     st_v2(row + (int64_t)vi * 8, make_uint2(packed[0], packed[1]));
@@ -542,15 +583,12 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 }
             }
             if constexpr (TR::token) {
-                if (tid == 0) reinterpret_cast<float*>(a.scales + (int64_t)d * a.scale_bytes)[0] = inv;
+                if (tid == 0) reinterpret_cast<float*>(a.scales + (int64_t)d * a.scale_bytes)[0] =
+                    __fdiv_rn(1.0f, s_tok);
             }
         }
     }
 }
-
-#ifndef EP_EXPERT_SCALED_VPT
-#define EP_EXPERT_SCALED_VPT 4   // 16-byte vectors per thread in the per-expert-scale kernel
-#endif
 
 #ifndef EP_DISPATCH_LAG
 #define EP_DISPATCH_LAG 4

@@ -3,9 +3,10 @@
 Tokens cycle through row kinds: plain, with +-inf planted, with NaNs of
 several payloads planted, all subnormal, all NaN, large values with -0, and
 zeros with one subnormal.  bf16 dispatch (per-expert and per-rank receive
-layouts) must move every bit pattern unchanged; per-token int8, static int8
-and the MX modes (no NaN rows: the MX and FP8 casts of NaN are not defined by
-the formulas) must match the oracle's codes and scales bit for bit; combine
+layouts) must move every bit pattern unchanged; per-token int8 (also with
+per-channel and per-expert input scales), static int8 and the MX modes (no
+NaN rows: the MX and FP8 casts of NaN are not defined by the formulas) must
+match the oracle's codes and scales bit for bit; combine
 must give NaN exactly where the oracle's float32 combine does, the same
 infinities, and finite values within the derived tolerance.
 """
@@ -96,6 +97,22 @@ def test_quantised_rows(q):
     assert np.array_equal(data.cpu().numpy(), od), "receive rows differ"
     if os_.shape[1]:
         assert np.array_equal(sc.cpu().numpy(), os_), "receive scales differ"
+
+
+@pytest.mark.parametrize("kind", [ep.EP_SCALES_PER_CHANNEL, ep.EP_SCALES_PER_EXPERT])
+def test_int8_with_input_scales(kind):
+    # subnormal rows times scales in [0.5, 2) stay subnormal: the infinite-scale path
+    w, topk, wts, x, olay, g = setup()
+    q = ep.EP_QUANT_INT8_PER_TOKEN
+    scales = synth.gen_scales(w, kind)
+    data, sc = g.lay.alloc_recv(q, olay.rows)
+    data.fill_(0xA5)
+    sc.fill_(0xA5)
+    g.lay.dispatch(to_dev_bf16(x), q, data, sc, scales=torch.from_numpy(scales).cuda(), scale_kind=kind)
+    od, os_ = oracle.dispatch_scaled(olay, x, q, topk, scales, kind)
+    assert g.lay.status() == ep.EP_OK
+    assert np.array_equal(data.cpu().numpy(), od), "receive rows differ"
+    assert np.array_equal(sc.cpu().numpy(), os_), "receive scales differ"
 
 
 def is_nan(b):
