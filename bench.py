@@ -83,6 +83,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="2", choices=sorted(WORKLOAD_KEYS))
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--graph", action="store_true",
+                   help="also time the step captured once in a CUDA graph and replayed")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work")
     p.add_argument("--tokens-per-rank", type=int, default=0,
@@ -397,6 +399,31 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
         phase["combine"].append(e[2].elapsed_time(e[3]))
     assert lay.status() == ep.EP_OK
 
+    # the same step captured once in a CUDA graph and replayed (launch cost
+    # out of the way: what a serving loop with small batches would see)
+    graph = None
+    if args.graph:
+        cap = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(cap):
+            step()
+        for _ in range(args.warmup):
+            cap.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            cap.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        assert lay.status() == ep.EP_OK
+        graph = {"ms": g0.elapsed_time(g1)}
+
     # end to end: pinned host buffers, copies in the timed region, pipelined
     # over three streams: copy-in of step i+1 and copy-out of step i-1 overlap
     # the kernels of step i; device input / output slots are double-buffered
@@ -488,7 +515,7 @@ def run_ours(args, w, quant, rank, local_rank, world, kind=0, mask_dims=0, recv_
     clocks = sampler.summary(t_timed0, t_timed1, t_warm0)
     bytes_ = algorithmic_bytes(w, quant, rows, V, per_rank, fmt, trows)
     return dict(total_ms=total_ms, phase=phase, e2e=e2e, clocks=clocks, bytes=bytes_, rows=rows,
-                V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_bf16, sh_dev=sh_dev)
+                V=V, x_host_bits=None, topk=topk, wts=wts, x_dev=x_bf16, sh_dev=sh_dev, graph=graph)
 
 
 def e2e_step_host(args, w, quant, lay, data, scales, y, topk, wts, x_dev, sh_dev, out, dev, barrier,
@@ -746,6 +773,12 @@ def main(argv=None):
                 "frac_of_peak": round(gbs[k] / peak, 4)} for k in avg},
         "rows": res["rows"], "valid_entries": res["V"],
     }
+    if res["graph"]:
+        gms = res["graph"]["ms"] / K
+        line["graph"] = {"ms_per_step": round(gms, 5), "value": round(world * w.N / (gms / 1e3), 1),
+                         "unit": "tokens/s", "steps": K,
+                         "note": "the same step captured once in a CUDA graph, replayed K times "
+                                 "(this rank; clocks not sampled for this part)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
