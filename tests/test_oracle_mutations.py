@@ -17,6 +17,7 @@ import test_oracle_dispatch_combine as tdc
 import test_oracle_formats as tfm
 import test_oracle_rms_norm as trn
 import test_oracle_layout as tl
+import test_oracle_nonfinite as tnf
 import test_oracle_quant as tq
 import test_oracle_quant_ext as tqx
 import test_oracle_token_layout as ttl
@@ -82,6 +83,13 @@ MUTANTS = {
                                   "double r = 1.0 / sqrt(ss / (double)(H - 1) + eps);"),
     "rms_gamma_shifted": ("x[n * H + h] * r * (double)oracle_bf16_to_f32(gamma[h]);",
                           "x[n * H + h] * r * (double)oracle_bf16_to_f32(gamma[(h + 1) % H]);"),
+    "int8_nan_enters_the_maximum": ("        if (a > amax) amax = a;\n    }\n    float s = 127.0f / amax;",
+                                    "        if (!(a <= amax)) amax = a;\n    }\n    float s = 127.0f / amax;"),
+    "int8_nan_product_not_zero": ("            if (r != r) r = 0.0f;   /* NaN product",
+                                  "            if (r != r) r = 127.0f;   /* NaN product"),
+    "int8_upper_clamp_dropped": ("            if (r > 127.0f) r = 127.0f;\n            if (r < -127.0f) r = -127.0f;",
+                                 "            if (r < -127.0f) r = -127.0f;"),
+    "mx_exponent_cap_too_low": ("if (se > 127) se = 127;", "if (se > 100) se = 100;"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -116,6 +124,10 @@ def pins():
     cases += [lambda s=s: tfm.test_dispatch_bytes_brute_force(s) for s in range(4)]
     cases += [lambda: tdc.test_expert_dequant_rows_more_modes(oracle.Q_FP8G_E4M3),
               lambda: tdc.test_expert_dequant_rows_more_modes(oracle.Q_INT8_STATIC)]
+    cases += [tnf.test_int8_infinite_element_zeroes_the_row, tnf.test_int8_subnormal_row_overflows_the_scale,
+              tnf.test_int8_nan_elements_are_skipped_and_coded_zero, tnf.test_int8_all_nan_row_is_the_zero_row,
+              tnf.test_int8_static_saturates_infinities_and_zeroes_nan, tnf.test_mx_block_with_infinity,
+              tnf.test_mx_all_subnormal_block]
     cases += [trn.test_hand_worked_row, lambda: trn.test_constant_row(1e-3, 1e-6),
               lambda: trn.test_constant_row(0.75, 1e-6), lambda: trn.test_matches_torch_rms_norm_float64(1e-6)]
     return cases
