@@ -234,6 +234,13 @@ ep_status ep_handle_status(const ep_handle* handle, ep_stream_t stream);
  *     largest finite value, scale byte = sharedExp + 127 (e8m0, the decode
  *     scale); e2m1 packs element 2i in the low nibble of byte i.
  * Each row is read once and quantised once, then written to its K rows.
+ * Non-finite input: every step is IEEE float32 arithmetic.  The row maximum
+ * skips NaN elements.  An infinite element gives s = 0, so the int8 codes
+ * are 0 and the scale word is +inf.  A row whose maximum is subnormal
+ * overflows s to +inf, so its codes are +-127 and 0 and the scale word is 0.
+ * A NaN product converts to int8 code 0.  An MX block holding +-inf takes
+ * sharedExp = 128 - emax and saturates the infinities.  The FP8/MX codes of a
+ * NaN element are unspecified.
  * Padding rows get all-zero data and scale bytes.  recv_data holds
  * recv_rows_capacity rows of ep_recv_row_bytes().data_bytes; recv_scales
  * holds as many rows of scale_bytes (NULL for NONE).  If the layout needs more
