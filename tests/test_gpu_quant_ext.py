@@ -86,6 +86,16 @@ def test_rows_not_multiple_of_16_bytes(q):
     run_case(synth.Workload(22, R=4, T=50, H=1000, E=16, K=3, alpha=4), q, kind)
 
 
+@pytest.mark.parametrize("q,H", [(ep.EP_QUANT_INT8_PER_TOKEN, 1000), (ep.EP_QUANT_FP8_E4M3_PER_TOKEN, 1000),
+                                 (ep.EP_QUANT_INT8_STATIC, 1000), (ep.EP_QUANT_FP8_E4M3_PER_GROUP, 1152),
+                                 (ep.EP_QUANT_INT8_PER_TOKEN, 8), (ep.EP_QUANT_FP8_E5M2_PER_TOKEN, 8184)])
+def test_per_expert_scales_ragged_rows(q, H):
+    # per-expert scales with rows that do not fill the last vectors of the CTA
+    # (H = 1000: 125 vectors on 32 threads x 4; H = 1152: 144 on 64 x 4), a
+    # single-warp CTA (H = 8) and the largest CTA with one vector short (H = 8184)
+    run_case(synth.Workload(24, R=4, T=40, H=H, E=16, K=4, alpha=4), q, 3)
+
+
 def test_zero_rows_and_groups():
     w = synth.Workload(23, R=2, T=6, H=256, E=4, K=2, alpha=1)
     topk = np.array([[[0, 1], [2, 3], [1, 2], [0, 3], [3, 1], [2, 0]]] * 2, np.int64)
