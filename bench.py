@@ -3,10 +3,12 @@
 routing -- layout (3 kernels) -> dispatch -> combine -- on one GPU holding all
 R logical expert-parallel ranks.
 
-Default workload: R=8 ranks x 4096 tokens, H=7168 bf16, 256 experts, top-8
-distinct uniform, softmax weights, alpha=1, no quantisation, identity experts
-(the combine reads the receive buffer).  ``--workload`` picks another one
-(1, 2, 3, 4a, 4b, 5) for local measurement; the default line is workload 2.
+Default workload (the largest that the path defines for one GPU): R=32 ranks x
+8192 tokens, H=4096 bf16, 512 experts, top-16 distinct uniform with 10 % of
+the entries -1, softmax weights over the valid entries, 4 shared-expert rows
+added in combine, alpha=64, no quantisation, identity experts (the combine
+reads the receive buffer).  ``--workload`` picks another one (1, 2, 3, 4a, 4b
+and the variants below) for local measurement.
 
 Prints one JSON line.  ``value`` is source tokens per second with inputs
 resident in HBM (inputs are larger than L2, so no flush is needed); ``e2e`` is
@@ -71,7 +73,12 @@ QNAME = {0: "none", 1: "int8_static", 2: "int8_per_token", 4: "mxfp8_e4m3", 5: "
 SCALE_KIND = {0: "none", 1: "scalar", 2: "per_channel", 3: "per_expert"}
 SAMPLE_NOTE = " (input scales and xActiveMask are not applied in the oracle sample)"
 FORMAT_NOTE = " (the oracle sample runs the plain path of the same mode, without the format variant)"
-KERNEL_SOURCES = {"dispatch": "dispatch.cu", "combine": "combine.cu", "layout": "layout.cu"}
+# sources whose code determines each phase's kernels (a profile counts only
+# while their digest is unchanged)
+PHASE_SOURCES = {"dispatch": ("dispatch.cu", "quant.cuh", "tma.cuh", "ep_internal.cuh"),
+                 "dispatch_scaled": ("dispatch_scaled.cu", "quant.cuh", "ep_internal.cuh"),
+                 "combine": ("combine.cu", "tma.cuh", "ep_internal.cuh"),
+                 "split": ("split.cu", "ep_internal.cuh")}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -81,7 +88,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="2", choices=sorted(WORKLOAD_KEYS))
+    p.add_argument("--workload", default="5", choices=sorted(WORKLOAD_KEYS))
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--graph", action="store_true",
                    help="also time the step captured once in a CUDA graph and replayed")
@@ -117,22 +124,33 @@ def code_text(src: str) -> str:
     return " ".join(src.split())
 
 
-def source_digest(name: str) -> str:
-    p = os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", name)
+def phase_files(phase: str, key: str) -> list:
+    """Source files of the kernels that make up a bench phase for a workload key."""
+    _, _, kind, _, _, fmt = WORKLOAD_KEYS[key]
+    if phase == "dispatch":
+        files = list(PHASE_SOURCES["dispatch_scaled" if kind == 3 else "dispatch"])
+    else:
+        files = list(PHASE_SOURCES[phase])
+    if fmt == "split":
+        files += [f for f in PHASE_SOURCES["split"] if f not in files]
+    return files
+
+
+def source_digest(files) -> str:
     h = hashlib.sha256()
-    for f in (p, os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", "ep_internal.cuh")):
-        with open(f, encoding="utf-8") as fh:
+    for name in files:
+        with open(os.path.join(ROOT, "combine_ep_layout_03_gb300", "csrc", name), encoding="utf-8") as fh:
             h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of that kernel; else None."""
+    """DRAM bytes per full-size launch from a committed ncu summary, if it was
+    taken on the current source of that phase's kernels; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    digest = source_digest(KERNEL_SOURCES[kernel])
+    digest = source_digest(phase_files(kernel, workload))
     pat = re.compile(r"^\|\s*%s\s*\|\s*%s\s*\|\s*([0-9]+)\s*\|\s*([0-9a-f]+)\s*\|" % (kernel, workload))
     with open(path) as f:
         for line in f:
@@ -727,7 +745,8 @@ def main(argv=None):
     med = {k: statistics.median(v) for k, v in res["phase"].items()}
     gbs = {k: res["bytes"][k] / (avg[k] / 1e3) / 1e9 for k in avg}
     dom = "dispatch" if avg["dispatch"] >= avg["combine"] else "combine"
-    traffic = profiled_traffic(dom, args.workload)
+    # the committed profiles hold DRAM bytes per full-size launch
+    traffic = None if args.tokens_per_rank else profiled_traffic(dom, args.workload)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(gbs[dom], 1), "peak": peak,
                 "unit": "GB/s", "frac": round(gbs[dom] / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"

@@ -13,8 +13,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libeplayout.so")
-SOURCES = ["ep_api.cu", "layout.cu", "dispatch.cu", "combine.cu", "split.cu", "noalloc.cu"]
-HEADERS = ["ep_internal.cuh", "tma.cuh"]
+SOURCES = ["ep_api.cu", "layout.cu", "dispatch.cu", "dispatch_scaled.cu", "combine.cu", "split.cu",
+           "noalloc.cu"]
+HEADERS = ["ep_internal.cuh", "tma.cuh", "quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -158,6 +158,7 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
             wn = a.w ? a.w[n * a.K + lane] : 1.0f;   // null weights: unit (per-rank rows)
         }
         bool ok = true;
+        int64_t armed = 0;   // work items whose stage this warp has armed (loads issued)
         for (int64_t j = 0; j < cnt && ok; ++j) {
             const int64_t n = blockIdx.x + j * G;
             const int d = dn;
@@ -199,9 +200,20 @@ combine_tma_kernel(CombineArgs a, CombineTma c) {
                               a.shared + ((sr * a.S + lane) * a.T + tt) * a.H + e0, cb, &full[s]);
                 if (NORM && lane == a.S)
                     bulk_load(st + (size_t)(kv + a.S) * rowb, a.residual + n * a.H + e0, cb, &full[s]);
+                armed = q + 1;
             }
         }
-        if (!ok && lane == 0) ep_set_status(a.status, EP_ERR_TIMEOUT);
+        if (lane == 0) {
+            if (!ok) ep_set_status(a.status, EP_ERR_TIMEOUT);
+            // Drain: the loads of the last arming of every stage land in this
+            // CTA's shared memory asynchronously.  Wait (bounded) until each has
+            // completed, so that the CTA never retires with a copy in flight,
+            // also when the consumers gave up on a wait and left early.  On the
+            // normal path the consumers wait for the same phases, so this adds
+            // no time.
+            for (int64_t q = armed > c.nstages ? armed - c.nstages : 0; q < armed; ++q)
+                mbar_wait(&full[q % c.nstages], (uint32_t)((q / c.nstages) & 1), a.max_polls);
+        }
         return;
     }
 

@@ -1,0 +1,208 @@
+// dispatch_scaled.cu -- dispatch with per-expert input scales (CANN
+// aclnnMoeDistributeDispatchV2, Formula, Cases 2-4 with scales of shape
+// (E, H)): each valid entry (s, t, k) receives x[s, t] * scales[e] encoded by
+// the mode's rule, e = topk[s, t, k], so a token is encoded once per
+// destination rather than once per token.
+#include "quant.cuh"
+
+namespace {
+
+#ifndef EP_EXPERT_SCALED_VPT
+#define EP_EXPERT_SCALED_VPT 4   // 16-byte vectors per thread in the per-expert-scale kernel
+#endif
+
+// Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
+// encoded once per destination with the scale row of that destination's
+// expert.  Warp 0 finds the experts of the valid destinations (bisection over
+// expert_base) and lists them compactly; each destination then takes one pass
+// over its scale-row slice (per-token modes add one CTA reduction of the row
+// maximum; each destination has its own reduction slot, so one barrier per
+// destination suffices) and every thread stores its codes directly.  The next
+// destination's scale slice is loaded into registers while the current one is
+// encoded, so its L2 latency overlaps the barrier and the stores.
+template <int Q, int VPT>
+__global__ void __launch_bounds__(1024 / VPT)
+dispatch_expert_scaled_kernel(DispatchArgs a) {
+    using TR = QTraits<Q>;
+    extern __shared__ int sbase[];   // [E+1] first row of each expert
+    __shared__ int sdst[kMaxTopk];
+    __shared__ int sexp[kMaxTopk];
+    __shared__ int snv;
+    // per-destination warp maxima, [destination][warp]; the slots of absent
+    // warps stay 0 so that a destination's slots are read four at a time
+    __shared__ __align__(16) uint32_t sred[kMaxTopk][32];
+    const int total = a.expert_base[a.E];
+    if ((int64_t)total > a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
+        return;
+    }
+    const int NT = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw4 = ((NT >> 5) + 3) >> 2;   // 16-byte groups of warp slots
+    for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
+    for (int i = tid; i < kMaxTopk * 32; i += NT) (&sred[0][0])[i] = 0u;
+    __syncthreads();
+    // this thread's scale slice of expert e: VPT x 2 float4
+    auto load_scales = [&](float4 (&sc)[VPT][2], int e) {
+        const float4* srow = reinterpret_cast<const float4*>(a.smooth + (int64_t)e * a.H);
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * NT + tid;
+            if (vi < a.nvec) {
+                sc[u][0] = __ldg(srow + 2 * vi);
+                sc[u][1] = __ldg(srow + 2 * vi + 1);
+            } else {
+                sc[u][0] = sc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    const int64_t items = a.N + a.E;
+    for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
+        if (w >= a.N) {
+            const int e = (int)(w - a.N);
+            const int64_t r0 = (int64_t)a.expert_base[e] + a.recv_cnt[e];
+            const int64_t r1 = a.expert_base[e + 1];
+            zero_rows(a, r0, r1);
+            continue;
+        }
+        __syncthreads();   // sdst / sexp / snv / sred of the previous token are consumed
+        if (warp == 0) {
+            const int d = lane < a.K ? a.dst_row[w * a.K + lane] : -1;
+            int lo = 0;
+            if (d >= 0) {
+                int hi = a.E;   // last expert e with sbase[e] <= d
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sbase[mid] <= d) lo = mid; else hi = mid;
+                }
+            }
+            const unsigned valid = __ballot_sync(kFull, d >= 0);
+            if (d >= 0) {
+                const int j = __popc(valid & ((1u << lane) - 1u));
+                sdst[j] = d;
+                sexp[j] = lo;
+            }
+            if (lane == 0) snv = __popc(valid);
+        }
+        const uint16_t* xrow = a.x + w * a.H;
+        float xf[VPT][8];   // the row as floats, unpacked once for all destinations
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * NT + tid;
+            unpack8(vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), xf[u]);
+        }
+        __syncthreads();
+        const int nvd = snv;
+        float4 sc[VPT][2];
+        if (nvd > 0) load_scales(sc, sexp[0]);
+        for (int j = 0; j < nvd; ++j) {
+            const int d = sdst[j];
+            float f[VPT][8];
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                f[u][0] = __fmul_rn(xf[u][0], sc[u][0].x); f[u][1] = __fmul_rn(xf[u][1], sc[u][0].y);
+                f[u][2] = __fmul_rn(xf[u][2], sc[u][0].z); f[u][3] = __fmul_rn(xf[u][3], sc[u][0].w);
+                f[u][4] = __fmul_rn(xf[u][4], sc[u][1].x); f[u][5] = __fmul_rn(xf[u][5], sc[u][1].y);
+                f[u][6] = __fmul_rn(xf[u][6], sc[u][1].z); f[u][7] = __fmul_rn(xf[u][7], sc[u][1].w);
+            }
+            if (j + 1 < nvd) load_scales(sc, sexp[j + 1]);   // overlaps the rest of this destination
+            float s_tok = 0.0f, amax = 0.0f;
+            if constexpr (TR::token) {
+                // row maximum: a tree over the thread's elements, one warp
+                // reduction instruction, then the warps' slots
+                float t[VPT];
+#pragma unroll
+                for (int u = 0; u < VPT; ++u) {
+                    const float a01 = fmaxf(fabsf(f[u][0]), fabsf(f[u][1]));
+                    const float a23 = fmaxf(fabsf(f[u][2]), fabsf(f[u][3]));
+                    const float a45 = fmaxf(fabsf(f[u][4]), fabsf(f[u][5]));
+                    const float a67 = fmaxf(fabsf(f[u][6]), fabsf(f[u][7]));
+                    t[u] = fmaxf(fmaxf(a01, a23), fmaxf(a45, a67));
+                }
+#pragma unroll
+                for (int w2 = 1; w2 < VPT; w2 <<= 1)
+#pragma unroll
+                    for (int u = 0; u + w2 < VPT; u += 2 * w2) t[u] = fmaxf(t[u], t[u + w2]);
+                // fmaxf returns the other operand for one NaN and NaN for two:
+                // the 0 operand makes an all-NaN slice 0, like a running maximum
+                uint32_t m = __float_as_uint(fmaxf(0.0f, t[0]));
+                m = __reduce_max_sync(kFull, m);
+                if (lane == 0) sred[j][warp] = m;
+                __syncthreads();
+                const uint4* slots = reinterpret_cast<const uint4*>(&sred[j][0]);
+                m = 0;
+                for (int i = 0; i < nw4; ++i) {
+                    const uint4 q4 = slots[i];
+                    m = max(m, max(max(q4.x, q4.y), max(q4.z, q4.w)));
+                }
+                amax = __uint_as_float(m);
+                s_tok = __fdiv_rn(TR::dmax, amax);
+            }
+            // int8 with a finite scale: |fl(f * s)| <= 127 (1 + 2^-24) for every
+            // element, so the rounded code is within +-127 and the clamp is
+            // idle; a NaN product converts to 0.  Only an infinite scale (a
+            // row whose maximum is subnormal, or zero) needs the clamped form.
+            const bool no_clamp = (Q == M_INT8) && amax > 0.0f && !isinf(s_tok);
+            uint8_t* row = a.data + (int64_t)d * a.row_bytes;
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                uint32_t packed[2], sb = 0;
+                float gi = 0.0f;
+                if (no_clamp) {
+                    const float* g = f[u];
+                    packed[0] = pack4_low_bytes(
+                        __float2int_rn(__fmul_rn(g[0], s_tok)), __float2int_rn(__fmul_rn(g[1], s_tok)),
+                        __float2int_rn(__fmul_rn(g[2], s_tok)), __float2int_rn(__fmul_rn(g[3], s_tok)));
+                    packed[1] = pack4_low_bytes(
+                        __float2int_rn(__fmul_rn(g[4], s_tok)), __float2int_rn(__fmul_rn(g[5], s_tok)),
+                        __float2int_rn(__fmul_rn(g[6], s_tok)), __float2int_rn(__fmul_rn(g[7], s_tok)));
+                } else {
+                    // the raw vector is only read by the MX modes, which take no input scales
+                    encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
+                }
+                const int vi = u * NT + tid;
+                if (vi < a.nvec) {
+                    st_v2(row + (int64_t)vi * 8, make_uint2(packed[0], packed[1]));
+                    if constexpr (TR::group) {
+                        if ((vi & 15) == 0) *reinterpret_cast<float*>(scale_at(a, d, vi >> 4)) = gi;
+                    }
+                }
+            }
+            if constexpr (TR::token) {
+                if (tid == 0) reinterpret_cast<float*>(a.scales + (int64_t)d * a.scale_bytes)[0] =
+                    __fdiv_rn(1.0f, s_tok);
+            }
+        }
+    }
+}
+
+template <int Q>
+cudaError_t launch_scaled_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
+    constexpr int EV = EP_EXPERT_SCALED_VPT;
+    const int ent = ((a.nvec + EV - 1) / EV + 31) / 32 * 32;
+    const size_t smem = sizeof(int) * (size_t)(a.E + 1);
+    int occ = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, dispatch_expert_scaled_kernel<Q, EV>, ent, smem);
+    if (err != cudaSuccess) return err;
+    const int64_t items = a.N + a.E;
+    int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
+    if (grid > items) grid = items;
+    if (grid < 1) grid = 1;
+    dispatch_expert_scaled_kernel<Q, EV><<<(unsigned)grid, ent, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_expert_scaled(const ep_handle* h, const DispatchArgs& a, int quant, cudaStream_t st) {
+    switch (quant) {
+        case M_INT8S: return launch_scaled_q<M_INT8S>(h, a, st);
+        case M_INT8: return launch_scaled_q<M_INT8>(h, a, st);
+        case M_FP8T_E4M3: return launch_scaled_q<M_FP8T_E4M3>(h, a, st);
+        case M_FP8T_E5M2: return launch_scaled_q<M_FP8T_E5M2>(h, a, st);
+        case M_FP8G_E4M3: return launch_scaled_q<M_FP8G_E4M3>(h, a, st);
+        case M_FP8G_E5M2: return launch_scaled_q<M_FP8G_E5M2>(h, a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}

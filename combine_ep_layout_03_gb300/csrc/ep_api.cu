@@ -26,22 +26,6 @@ bool valid_quant(int q) {
 // quantModes 1-3 take input scales; NONE and MX take none
 bool takes_scales(int q) { return q != EP_QUANT_NONE && !is_mx(q); }
 
-struct Tiling { int32_t C, TPB, B; };
-
-Tiling tiling_of(const ep_params* p) {
-    Tiling t;
-    const int R = p->num_ranks, T = p->tokens_per_rank;
-    if (T == 0) { t.C = 1; t.TPB = 0; t.B = R; return t; }
-    int C = (kLayoutTargetBlocks + R - 1) / R;
-    const int max_c = (T + 31) / 32;  // at least 32 tokens per CTA
-    if (C > max_c) C = max_c;
-    if (C < 1) C = 1;
-    t.TPB = (T + C - 1) / C;
-    t.C = (T + t.TPB - 1) / t.TPB;
-    t.B = R * t.C;
-    return t;
-}
-
 int64_t worst_rows(const ep_params* p) {
     return (int64_t)p->num_ranks * p->tokens_per_rank * p->topk +
            (int64_t)p->num_experts * (p->expert_alignment - 1);

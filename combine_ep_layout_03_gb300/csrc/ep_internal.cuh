@@ -20,6 +20,26 @@ constexpr int kDispatchSmemBudget = 200 * 1024;  // shared-memory ring of the bu
 #endif
 constexpr int kCombineSmemBudget = EP_COMBINE_SMEM_BUDGET;
 
+// Layout tiling of a problem: C CTAs per source rank, TPB tokens per CTA,
+// B = R * C CTAs in all (at least 32 tokens per CTA, about
+// kLayoutTargetBlocks CTAs).  ep_layout and ep_layout_static_scratch both size
+// their per-CTA scratch from it.
+struct Tiling { int32_t C, TPB, B; };
+
+inline Tiling tiling_of(const ep_params* p) {
+    Tiling t;
+    const int R = p->num_ranks, T = p->tokens_per_rank;
+    if (T == 0) { t.C = 1; t.TPB = 0; t.B = R; return t; }
+    int C = (kLayoutTargetBlocks + R - 1) / R;
+    const int max_c = (T + 31) / 32;  // at least 32 tokens per CTA
+    if (C > max_c) C = max_c;
+    if (C < 1) C = 1;
+    t.TPB = (T + C - 1) / C;
+    t.C = (T + t.TPB - 1) / t.TPB;
+    t.B = R * t.C;
+    return t;
+}
+
 struct ep_handle {
     ep_params p;
     int32_t R, T, H, E, K, L, alpha;

@@ -23,7 +23,11 @@
 // names a host-side stand-in).  The first call on each device therefore asks
 // the runtime for the array's device address with cudaGetSymbolAddress, with
 // that device current, and caches it per device; make that first call before
-// any stream capture begins.
+// any stream capture begins.  The cached address belongs to the device's
+// primary context as it was at that first call: after cudaDeviceReset (or
+// anything else that destroys the primary context) the module is loaded
+// afresh, the cached address is stale, and this entry point must not be
+// called again in that process.
 #include <atomic>
 #include <mutex>
 
@@ -68,6 +72,13 @@ extern "C" ep_status ep_layout_static_scratch(const ep_params* p, const int64_t*
         !o->recv_cnt || !o->aligned_cnt || !o->expert_start || !o->rank_base || !o->expert_base ||
         !o->src_prefix || !o->expert_ids || !o->expert_usage_stats)
         return EP_ERR_INVALID_ARG;
+    // outputs are written as int32 / int64 words: misaligned arrays are refused
+    const void* words[] = {o->status, o->cnt, o->num_tokens_per_rank, o->recv_cnt, o->aligned_cnt,
+                           o->expert_start, o->expert_base, o->src_prefix, o->dst_row, o->recv_src,
+                           o->expert_ids, o->expert_usage_stats};
+    for (const void* w : words)
+        if (((uintptr_t)w % 4) != 0) return EP_ERR_INVALID_ARG;
+    if (((uintptr_t)o->rank_base % 8) != 0) return EP_ERR_INVALID_ARG;
 
     ep_handle h{};
     h.p = *p;
@@ -77,21 +88,14 @@ extern "C" ep_status ep_layout_static_scratch(const ep_params* p, const int64_t*
     h.recv_cap = p->recv_capacity_rows > 0
                      ? p->recv_capacity_rows
                      : h.N * h.K + (int64_t)h.E * (h.alpha - 1);
-    if (h.N > 0 && (!topk || !o->dst_row)) return EP_ERR_INVALID_ARG;
+    // topk_idx is read as int64 words: a misaligned pointer is refused here,
+    // before any launch, as ep_layout_masked does
+    if (h.N > 0 && (!topk || ((uintptr_t)topk % 8) != 0 || !o->dst_row)) return EP_ERR_INVALID_ARG;
     if (h.recv_cap > 0 && !o->recv_src) return EP_ERR_INVALID_ARG;
 
     // the same tiling as ep_layout: CTAs own contiguous token ranges of one rank
-    if (h.T == 0) {
-        h.C = 1; h.TPB = 0;
-    } else {
-        int C = (kLayoutTargetBlocks + h.R - 1) / h.R;
-        const int max_c = (h.T + 31) / 32;
-        if (C > max_c) C = max_c;
-        if (C < 1) C = 1;
-        h.TPB = (h.T + C - 1) / C;
-        h.C = (h.T + h.TPB - 1) / h.TPB;
-    }
-    h.B = h.R * h.C;
+    const Tiling t = tiling_of(p);
+    h.C = t.C; h.TPB = t.TPB; h.B = t.B;
     const size_t hist_bytes = round_up(sizeof(int32_t) * (size_t)h.B * h.E);
     const size_t rank_bytes = round_up(sizeof(int32_t) * (size_t)h.B * h.R);
     if (hist_bytes + rank_bytes > kEpStaticScratchBytes) return EP_ERR_UNSUPPORTED;

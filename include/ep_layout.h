@@ -537,13 +537,20 @@ typedef struct ep_layout_outputs {
  * The caller passes topk_idx and every output array; the call allocates
  * nothing.  The layout's scratch (per-CTA histograms) lives in a fixed 2 MiB
  * device array owned by the library, present on every GPU that loads it until
- * the process exits.  Problems whose scratch exceeds 2 MiB (about 608 CTAs x
- * (E + R) x 4 bytes) return EP_ERR_UNSUPPORTED before any launch.  All calls
- * share the array: calls whose kernels may overlap on the GPU race and must be
- * serialised by the caller.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  Status values as for ep_layout,
- * written to outputs->status. */
+ * the process exits.  A problem's scratch is B x E x 4 bytes plus B x R x 4
+ * bytes, each rounded up to a multiple of 256, for B = R x C layout CTAs with
+ * C = max(1, min(ceil(608 / R), ceil(T / 32))); B can reach nearly twice 608
+ * when R does not divide 608 (R = 512 gives B = 1024).  Problems whose scratch
+ * exceeds 2 MiB return EP_ERR_UNSUPPORTED before any launch.  topk_idx and
+ * rank_base must be 8-byte aligned and the other outputs 4-byte aligned, else
+ * EP_ERR_INVALID_ARG before any launch.  All calls share the array: calls
+ * whose kernels may overlap on the GPU race and must be serialised by the
+ * caller.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  The cached address does not survive cudaDeviceReset: after
+ * the primary context is reset, do not call this entry point again in the
+ * same process.  Status values as for ep_layout, written to
+ * outputs->status. */
 ep_status ep_layout_static_scratch(const ep_params* params, const int64_t* topk_idx,
                                    const ep_layout_outputs* outputs, ep_stream_t stream);
 

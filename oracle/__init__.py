@@ -109,6 +109,7 @@ def _declare(lib):
     lib.oracle_reduce_token_weights.argtypes = [i64, i32, vp, vp, vp]
     lib.oracle_dispatch_bytes.argtypes = [i32, i32, vp, vp, i64, i64, i64, vp]
     lib.oracle_encode_row.argtypes = [i32, i32, vp, vp, vp]
+    lib.oracle_encode_rows.argtypes = [i32, i32, i64, vp, vp, vp]
     lib.oracle_add_rms_norm_ref64.argtypes = [i64, i32, vp, vp, vp, ctypes.c_double, vp, vp, vp]
     return lib
 
@@ -210,6 +211,34 @@ def encode_row(q: int, x_bf16: np.ndarray, smooth=None):
         assert q in (Q_INT8_STATIC, Q_INT8, Q_FP8T_E4M3, Q_FP8T_E5M2, Q_FP8G_E4M3, Q_FP8G_E5M2)
         load().oracle_encode_row_scaled(q, H, _p(x), _p(_scale_arr(smooth, H)), _p(data), _p(scale))
     return data, scale[:sb]
+
+
+def encode_rows(q: int, x_bf16: np.ndarray, threads: int = 1):
+    """Receive-row bytes (data [n, db], scales [n, sb]) of every source row of
+    x [n, H], each encoded once (the per-token encoding of dispatch).  With
+    threads > 1, contiguous chunks of rows are encoded on that many threads at
+    once (the C calls release the interpreter lock and share no state)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    H = x.shape[-1]
+    x = x.reshape(-1, H)
+    n = x.shape[0]
+    db, sb = row_bytes(q, H)
+    data = np.empty((n, db), np.uint8)
+    scales = np.empty((n, sb), np.uint8)
+    lib = load()
+
+    def part(a, b):
+        if b > a:
+            lib.oracle_encode_rows(q, H, b - a, _p(x[a:b]), _p(data[a:b]), _p(scales[a:b]) if sb else None)
+
+    if threads <= 1 or n < 2 * threads:
+        part(0, n)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        step = -(-n // threads)
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda a: part(a, min(n, a + step)), range(0, n, step)))
+    return data, scales
 
 
 # ---------------------------------------------------------------------------
@@ -314,10 +343,13 @@ def dispatch_scaled(lay: Layout, x_bf16: np.ndarray, q: int, topk: np.ndarray,
     return data, scl
 
 
-def dispatch_bytes(lay, src_rows: np.ndarray, rows: int | None = None) -> np.ndarray:
+def dispatch_bytes(lay, src_rows: np.ndarray, rows: int | None = None, row_begin: int = 0,
+                   out: np.ndarray | None = None) -> np.ndarray:
     """Scatter of already-encoded source rows [N, nbytes] (uint8) onto the
-    receive rows of a layout (lay.dst_row, or a TokenLayout's tok_dst); rows
-    that no entry reaches are zero.  rows defaults to the layout's row count."""
+    receive rows [row_begin, rows) of a layout (lay.dst_row, or a TokenLayout's
+    tok_dst); rows that no entry reaches are zero.  rows defaults to the
+    layout's row count.  out, when given, is a [rows - row_begin, nbytes]
+    uint8 buffer to fill (a large receive buffer can be built rank by rank)."""
     N = lay.R * lay.T
     src = np.ascontiguousarray(src_rows, dtype=np.uint8).reshape(N, -1) if N else \
         np.zeros((0, np.shape(src_rows)[-1]), np.uint8)
@@ -325,9 +357,11 @@ def dispatch_bytes(lay, src_rows: np.ndarray, rows: int | None = None) -> np.nda
     dst = lay.tok_dst if hasattr(lay, "tok_dst") else lay.dst_row
     if rows is None:
         rows = lay.rows
-    out = np.zeros((rows, nb), np.uint8)
+    if out is None:
+        out = np.zeros((rows - row_begin, nb), np.uint8)
+    assert out.shape == (rows - row_begin, nb) and out.dtype == np.uint8 and out.flags.c_contiguous
     dr = np.ascontiguousarray(dst.reshape(-1), dtype=np.int32)
-    load().oracle_dispatch_bytes(N, lay.K, _p(dr), _p(src), nb, 0, rows, _p(out))
+    load().oracle_dispatch_bytes(N, lay.K, _p(dr), _p(src), nb, row_begin, rows, _p(out))
     return out
 
 

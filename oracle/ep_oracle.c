@@ -334,6 +334,15 @@ void oracle_encode_row(int q, int H, const uint16_t* x, uint8_t* data, uint8_t* 
     else oracle_encode_row_scaled(q, H, x, NULL, data, scale);
 }
 
+/* Encode n consecutive source rows (rows of H bf16 elements) with
+ * oracle_encode_row: the per-token encoding that dispatch copies to each of
+ * the token's receive rows. */
+void oracle_encode_rows(int q, int H, int64_t n, const uint16_t* x, uint8_t* data, uint8_t* scales) {
+    int64_t db = oracle_row_data_bytes(q, H), sb = oracle_row_scale_bytes(q, H);
+    for (int64_t i = 0; i < n; ++i)
+        oracle_encode_row(q, H, x + i * H, data + i * db, sb ? scales + i * sb : NULL);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Routing layout.                                                          */
 /*                                                                          */

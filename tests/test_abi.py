@@ -310,3 +310,25 @@ def test_step_host_validation():
     assert L.ep_step_host(h, 0, None, B, C, None, 0, D, ref, None) == ep.EP_ERR_INVALID_ARG    # no host topk
     assert L.ep_step_host(h, 11, A, B, C, None, 0, D, ref, None) == ep.EP_ERR_UNSUPPORTED
     ep.ep_handle_destroy(h)
+
+
+def test_static_scratch_layout_refuses_misaligned_pointers_before_any_launch():
+    p = ep.make_params(2, 8, 64, 4, 2, 1, 0)
+    L = ep.lib
+    names = [n for n, _ in ep.ep_layout_outputs._fields_]
+
+    def outputs(**override):
+        vals = {n: (1 << 40) + (i << 20) for i, n in enumerate(names)}   # aligned stand-ins
+        vals.update(override)
+        return ctypes.byref(ep.ep_layout_outputs(**vals))
+
+    topk_ok = 1 << 44
+    # topk_idx is read as int64 words
+    for off in (1, 4):
+        assert L.ep_layout_static_scratch(p, topk_ok + off, outputs(), None) == ep.EP_ERR_INVALID_ARG
+    # int32 outputs need 4-byte and rank_base 8-byte alignment
+    assert L.ep_layout_static_scratch(p, topk_ok, outputs(dst_row=(1 << 40) + 2), None) == \
+        ep.EP_ERR_INVALID_ARG
+    assert L.ep_layout_static_scratch(p, topk_ok, outputs(rank_base=(1 << 40) + 4), None) == \
+        ep.EP_ERR_INVALID_ARG
+    assert L.ep_layout_static_scratch(p, topk_ok, outputs(status=None), None) == ep.EP_ERR_INVALID_ARG

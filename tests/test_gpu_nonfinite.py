@@ -6,7 +6,9 @@ zeros with one subnormal.  bf16 dispatch (per-expert and per-rank receive
 layouts) must move every bit pattern unchanged; per-token int8 (also with
 per-channel and per-expert input scales), static int8 and the MX modes (no
 NaN rows: the MX and FP8 casts of NaN are not defined by the formulas) must
-match the oracle's codes and scales bit for bit; combine
+match the oracle's codes and scales bit for bit; MX rows holding NaN
+elements must match the oracle's scale bytes and the codes of every non-NaN
+element (a NaN element's own code is left unspecified); combine
 must give NaN exactly where the oracle's float32 combine does, the same
 infinities, and finite values within the derived tolerance.
 """
@@ -97,6 +99,28 @@ def test_quantised_rows(q):
     assert np.array_equal(data.cpu().numpy(), od), "receive rows differ"
     if os_.shape[1]:
         assert np.array_equal(sc.cpu().numpy(), os_), "receive scales differ"
+
+
+@pytest.mark.parametrize("q", [ep.EP_QUANT_MXFP8_E4M3, ep.EP_QUANT_MXFP8_E5M2, ep.EP_QUANT_MXFP4_E2M1])
+def test_mx_blocks_with_nan_elements(q):
+    w, topk, wts, x, olay, g = setup(nan_rows=True)
+    data, sc = g.lay.alloc_recv(q, olay.rows)
+    data.fill_(0xA5)
+    sc.fill_(0xA5)
+    g.lay.dispatch(to_dev_bf16(x), q, data, sc)
+    od, os_ = oracle.dispatch(olay, x, q)
+    assert g.lay.status() == ep.EP_OK
+    assert np.array_equal(sc.cpu().numpy(), os_), "scale bytes differ"
+    src = olay.recv_src[: olay.rows]
+    assert np.all(src >= 0)
+    nan = is_nan(x)[src]                                # [rows, H] NaN source elements
+    got = data.cpu().numpy()
+    if q == ep.EP_QUANT_MXFP4_E2M1:
+        # element 2i in the low nibble of byte i
+        got = np.stack([got & 0xF, got >> 4], axis=-1).reshape(nan.shape)
+        od = np.stack([od & 0xF, od >> 4], axis=-1).reshape(nan.shape)
+    assert nan.any() and (~nan).any()
+    assert np.array_equal(got[~nan], od[~nan]), "codes of non-NaN elements differ"
 
 
 @pytest.mark.parametrize("kind", [ep.EP_SCALES_PER_CHANNEL, ep.EP_SCALES_PER_EXPERT])

@@ -81,6 +81,31 @@ def test_encode_then_move_equals_fused_dispatch(q):
         assert np.array_equal(oracle.dispatch_bytes(lay, src_s), fused_s)
 
 
+@pytest.mark.parametrize("q", [oracle.Q_NONE, oracle.Q_INT8, oracle.Q_E4M3, oracle.Q_E2M1,
+                               oracle.Q_FP8G_E4M3])
+@pytest.mark.parametrize("threads", [1, 3])
+def test_encode_rows_then_ranked_moves_equal_fused_dispatch(q, threads):
+    """The batch encoder with a rank-by-rank scatter (as the full-size GPU
+    parity builds the receive buffer) equals the oracle's fused dispatch."""
+    w = synth.WORKLOADS[3].with_(T=40, H=256)       # Zipf routing, alpha = 128: padding rows
+    topk = synth.gen_topk(w)
+    x = synth.gen_x(w).reshape(w.R * w.T, w.H)
+    lay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    enc_d, enc_s = oracle.encode_rows(q, x, threads)
+    for n in (0, 7, w.R * w.T - 1):
+        d1, s1 = oracle.encode_row(q, x[n])
+        assert np.array_equal(enc_d[n], d1) and np.array_equal(enc_s[n], s1)
+    fused_d, fused_s = oracle.dispatch(lay, x, q)
+    db, sb = oracle.row_bytes(q, w.H)
+    for j in range(w.R):
+        a, b = int(lay.rank_base[j]), int(lay.rank_base[j + 1])
+        buf = np.full((b - a, db), 0xA5, np.uint8)
+        oracle.dispatch_bytes(lay, enc_d, rows=b, row_begin=a, out=buf)
+        assert np.array_equal(buf, fused_d[a:b])
+        if sb:
+            assert np.array_equal(oracle.dispatch_bytes(lay, enc_s, rows=b, row_begin=a), fused_s[a:b])
+
+
 def test_transpose_scales_hand_worked():
     rows = np.array([[1, 2, 3], [4, 5, 6]], np.uint8)
     expect = np.array([[1, 4, 0, 0], [2, 5, 0, 0], [3, 6, 0, 0]], np.uint8)

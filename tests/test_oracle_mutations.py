@@ -90,6 +90,8 @@ MUTANTS = {
     "int8_upper_clamp_dropped": ("            if (r > 127.0f) r = 127.0f;\n            if (r < -127.0f) r = -127.0f;",
                                  "            if (r < -127.0f) r = -127.0f;"),
     "mx_exponent_cap_too_low": ("if (se > 127) se = 127;", "if (se > 100) se = 100;"),
+    "mx_nan_enters_the_block_maximum": ("            if (a > amax) amax = a;\n        }\n        int expfield",
+                                        "            if (!(a <= amax)) amax = a;\n        }\n        int expfield"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -127,7 +129,8 @@ def pins():
     cases += [tnf.test_int8_infinite_element_zeroes_the_row, tnf.test_int8_subnormal_row_overflows_the_scale,
               tnf.test_int8_nan_elements_are_skipped_and_coded_zero, tnf.test_int8_all_nan_row_is_the_zero_row,
               tnf.test_int8_static_saturates_infinities_and_zeroes_nan, tnf.test_mx_block_with_infinity,
-              tnf.test_mx_all_subnormal_block]
+              tnf.test_mx_all_subnormal_block, tnf.test_mx_block_maximum_skips_nan,
+              tnf.test_mx_block_of_nan_only_takes_the_smallest_exponent]
     cases += [trn.test_hand_worked_row, lambda: trn.test_constant_row(1e-3, 1e-6),
               lambda: trn.test_constant_row(0.75, 1e-6), lambda: trn.test_matches_torch_rms_norm_float64(1e-6)]
     return cases

@@ -15,7 +15,11 @@ step (the reading kept for every mode whose result stays well defined):
 - MX (quantMode 4): a block holding +-inf has the exponent field 255, so
   sharedExp = 128 - emax, and the infinities saturate to the largest finite
   code; finite elements of that block shrink by 2^-(128 - emax) and round to
-  (signed) zero unless large; an all-subnormal block takes sharedExp = -127.
+  (signed) zero unless large; an all-subnormal block takes sharedExp = -127;
+  the block maximum skips NaN elements (the same running greater-than
+  maximum), so a block's scale byte and its finite elements' codes come from
+  its non-NaN elements alone, and a block of NaN only has sharedExp = -127.
+  The code of a NaN element itself is left unspecified.
 
 Every expected value below is worked from those rules and the format
 definitions by hand, not produced by the oracle.
@@ -103,3 +107,38 @@ def test_mx_all_subnormal_block():
     codes, sc = oracle.quant_mx_row(6, x)
     assert list(sc) == [0]
     assert list(codes[:1]) == [0x80]
+
+
+MINUS_0_296875 = 0xBE98   # -1.1875 * 2^-2, exact in bf16
+
+
+def test_mx_block_maximum_skips_nan():
+    # non-NaN elements: 1.0, -0.296875, 0.5 -> amax 1.0 (unbiased exponent 0);
+    # the NaN payloads (magnitude bits above infinity's) take no part
+    x = row([QNAN, ONE, MINUS_0_296875, NAN_LOW, NNAN, HALF])
+    finite = [1, 2, 5]
+    # e4m3: sharedExp = 0 - 8 = -8, byte 119 = 0x77; 1.0 * 2^8 = 256 = 0x78;
+    # -76 ties between 72 and 80, even mantissa 80 -> 0xEA; 0.5 * 2^8 = 128 = 0x70
+    codes, sc = oracle.quant_mx_row(4, x)
+    assert list(sc) == [0x77]
+    assert [codes[i] for i in finite] == [0x78, 0xEA, 0x70]
+    assert np.all(codes[6:] == 0)
+    # e5m2: sharedExp = -15, byte 112 = 0x70; 2^15 -> exponent field 30 = 0x78;
+    # -9728 = -1.1875 * 2^13 rounds to -1.25 * 2^13 = 0xF1; 2^14 = 0x74
+    codes, sc = oracle.quant_mx_row(5, x)
+    assert list(sc) == [0x70]
+    assert [codes[i] for i in finite] == [0x78, 0xF1, 0x74]
+    # e2m1: sharedExp = -2, byte 125 = 0x7D; 4 = 0x6, -1.1875 -> -1.0 = 0xA,
+    # 2 = 0x4 (element 2i in the low nibble of byte i)
+    codes, sc = oracle.quant_mx_row(6, x)
+    assert list(sc) == [0x7D]
+    nib = [(codes[i // 2] >> (4 * (i & 1))) & 0xF for i in finite]
+    assert nib == [0x6, 0xA, 0x4]
+
+
+def test_mx_block_of_nan_only_takes_the_smallest_exponent():
+    x = np.full(32, QNAN, np.uint16)
+    x[7] = NNAN
+    for q in (4, 5, 6):
+        _, sc = oracle.quant_mx_row(q, x)
+        assert list(sc) == [0]
