@@ -111,6 +111,7 @@ def _declare(lib):
     lib.oracle_encode_row.argtypes = [i32, i32, vp, vp, vp]
     lib.oracle_encode_rows.argtypes = [i32, i32, i64, vp, vp, vp]
     lib.oracle_add_rms_norm_ref64.argtypes = [i64, i32, vp, vp, vp, ctypes.c_double, vp, vp, vp]
+    lib.oracle_add_rms_norm_f32.argtypes = [i64, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp]
     return lib
 
 
@@ -611,6 +612,22 @@ def add_rms_norm_ref64(c: np.ndarray, residual_bf16: np.ndarray, gamma_bf16: np.
     rstd = np.zeros(N, np.float64)
     y = np.zeros((N, H), np.float64)
     load().oracle_add_rms_norm_ref64(N, H, _p(c), _p(r), _p(g), float(eps), _p(x), _p(rstd), _p(y))
+    return x, rstd, y
+
+
+def add_rms_norm_f32(c_bf16: np.ndarray, residual_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float):
+    """(x bf16 bits, rstd float32, y bf16 bits) of the AddRmsNorm taken step by
+    step in binary32 from the combine's bf16 output c [N, H]: x = fl32(c + r),
+    a left-to-right binary32 sum of squares, rstd = 1/sqrt(sum/H + eps),
+    y = bf16((x * rstd) * gamma)."""
+    c = np.ascontiguousarray(c_bf16, dtype=np.uint16)
+    N, H = c.shape
+    r = np.ascontiguousarray(residual_bf16, dtype=np.uint16).reshape(N, H)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16).reshape(H)
+    x = np.zeros((N, H), np.uint16)
+    rstd = np.zeros(N, np.float32)
+    y = np.zeros((N, H), np.uint16)
+    load().oracle_add_rms_norm_f32(N, H, _p(c), _p(r), _p(g), float(eps), _p(x), _p(rstd), _p(y))
     return x, rstd, y
 
 

@@ -818,3 +818,37 @@ void oracle_add_rms_norm_ref64(int64_t N, int H, const double* c, const uint16_t
             y[n * H + h] = x[n * H + h] * r * (double)oracle_bf16_to_f32(gamma[h]);
     }
 }
+
+/* The same AddRmsNorm step by step in binary32, from the combine's output
+ * rounded to bf16 (the reading of CANN aclnnMoeDistributeCombineAddRmsNorm
+ * taken for the fused combine, which first rounds the weighted sum to the
+ * combine's bf16 output):
+ *   x    = fl32(c + residual)                  c, residual: bf16 values
+ *   ss   = sum over h of fl32(x_h * x_h), added left to right in binary32
+ *   rstd = fl32(1 / fl32(sqrt(fl32(fl32(ss / H) + eps))))
+ *   y    = bf16(fl32(fl32(x * rstd) * gamma))
+ * Outputs bf16(x), rstd and y.  sqrtf is IEEE's correctly rounded square
+ * root.  Any summation order is an equally valid reading of "mean"; this one
+ * is the plainest. */
+void oracle_add_rms_norm_f32(int64_t N, int H, const uint16_t* c, const uint16_t* residual,
+                             const uint16_t* gamma, float eps, uint16_t* x_out, float* rstd, uint16_t* y) {
+    float* x = (float*)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+    for (int64_t n = 0; n < N; ++n) {
+        float ss = 0.0f;
+        for (int h = 0; h < H; ++h) {
+            float v = oracle_bf16_to_f32(c[n * H + h]) + oracle_bf16_to_f32(residual[n * H + h]);
+            x[h] = v;
+            x_out[n * H + h] = oracle_bf16_from_f32(v);
+            float sq = v * v;
+            ss = ss + sq;
+        }
+        float mean = ss / (float)H;
+        float r = 1.0f / sqrtf(mean + eps);
+        rstd[n] = r;
+        for (int h = 0; h < H; ++h) {
+            float t = x[h] * r;
+            y[n * H + h] = oracle_bf16_from_f32(t * oracle_bf16_to_f32(gamma[h]));
+        }
+    }
+    free(x);
+}

@@ -4,6 +4,12 @@ aclnnMoeDistributeCombineAddRmsNorm) against the oracle.
 - x_out, rstd and y within the tolerance derived in the oracle (combine
   rounded to bf16, residual added and normalised in float32) of the float64
   reference built from the oracle's own layout, dispatch and stand-in expert;
+- the oracle's float32 steps of the same reading (combine rounded to bf16,
+  residual added in float32, a float32 sum of squares, rstd, two float32
+  products): wherever the oracle's bf16 combine equals the GPU's plain
+  combine (the combine's float32 summation order differs, so not quite
+  everywhere), x_out equals the oracle's bit for bit and y is within one bf16
+  step of it; rstd is within the float32 summation-order bound;
 - the composition: x_out equals, bit for bit, bf16(float32(c) + residual) with
   c the plain combine's output of the same kernel arithmetic;
 - edges: no tokens, tokens without experts, a receive buffer that is too small;
@@ -52,11 +58,37 @@ def run_norm(w, quant=0, mark=4, check_composition=True):
     ok, worst = oracle.add_rms_norm_within_tolerance(bf16_bits(x_out), rstd.cpu().numpy(), bf16_bits(out),
                                                      ref, w.K, w.num_shared)
     assert ok, worst
+    c = g.combine(y, wts_dev, sh_dev)
     if check_composition:
-        c = g.combine(y, wts_dev, sh_dev)
         xf = (c.float() + res_dev.float()).to(torch.bfloat16)
         assert torch.equal(xf.view(torch.int16), x_out.view(torch.int16))
+    # the oracle's float32 steps from its own bf16 combine
+    c_or = oracle.combine(olay, oy, wts, shared)
+    xo, ro, yo = oracle.add_rms_norm_f32(c_or, res.reshape(w.N, w.H), gam, EPS)
+    check_against_f32_steps(bf16_bits(c), c_or, bf16_bits(x_out), xo, rstd.cpu().numpy(), ro,
+                            bf16_bits(out), yo, w.H)
     return worst
+
+
+def check_against_f32_steps(c_gpu, c_or, x_gpu, x_or, r_gpu, r_or, y_gpu, y_or, H, min_match=0.99):
+    """Bit-exact x_out where the bf16 combines agree; rstd within the float32
+    summation-order bound ((H + 8) 2^-24 relative: both sides add H positive
+    squares, in different orders); y within one bf16 step where the combines
+    agree (a relative rstd difference that small moves a product by less than
+    one bf16 step, so at most one rounding flips)."""
+    N = c_gpu.shape[0]
+    c_gpu, c_or = c_gpu.reshape(N, H), c_or.reshape(N, H)
+    match = c_gpu == c_or
+    if match.size:
+        assert match.mean() >= min_match, f"only {match.mean():.4f} of the combines agree"
+    assert np.array_equal(x_gpu.reshape(N, H)[match], x_or[match]), "x_out differs where the combines agree"
+    r_gpu = np.asarray(r_gpu, np.float64)
+    r_or = np.asarray(r_or, np.float64)
+    assert np.all(np.abs(r_gpu - r_or) <= (H + 8) * 2.0 ** -24 * r_or), "rstd outside the bound"
+    yg = oracle.bf16_bits_to_f64(y_gpu.reshape(N, H))
+    yr = oracle.bf16_bits_to_f64(y_or.reshape(N, H))
+    step = oracle.ulp_bf16(np.maximum(np.abs(yg), np.abs(yr)))
+    assert np.all(np.abs(yg - yr)[match] <= step[match]), "y more than one bf16 step from the oracle's"
 
 
 @pytest.mark.parametrize("idx,T,quant", [(1, 64, 0), (1, 64, 4), (2, 48, 0), (3, 40, 2), (5, 12, 0)])
@@ -124,3 +156,9 @@ def test_full_size_workload2_sampled():
     ok, worst = oracle.add_rms_norm_within_tolerance(bf16_bits(x_out[tk]), rstd[tk].cpu().numpy(),
                                                      bf16_bits(out[tk]), ref, w.K, 0)
     assert ok, worst
+    # float32 steps of the oracle on the sampled tokens
+    c_gpu = g.combine(y, torch.from_numpy(wts).cuda())
+    c_or, _, _ = oracle_combine_sampled(olay, x, wts, None, 0, 0, tokens)
+    xo, ro, yo = oracle.add_rms_norm_f32(c_or, bf16_bits(res_dev[tk]), gam, EPS)
+    check_against_f32_steps(bf16_bits(c_gpu[tk]), c_or, bf16_bits(x_out[tk]), xo, rstd[tk].cpu().numpy(), ro,
+                            bf16_bits(out[tk]), yo, w.H)

@@ -92,6 +92,13 @@ MUTANTS = {
     "mx_exponent_cap_too_low": ("if (se > 127) se = 127;", "if (se > 100) se = 100;"),
     "mx_nan_enters_the_block_maximum": ("            if (a > amax) amax = a;\n        }\n        int expfield",
                                         "            if (!(a <= amax)) amax = a;\n        }\n        int expfield"),
+    "rms32_residual_dropped": (
+        "float v = oracle_bf16_to_f32(c[n * H + h]) + oracle_bf16_to_f32(residual[n * H + h]);",
+        "float v = oracle_bf16_to_f32(c[n * H + h]);"),
+    "rms32_eps_outside_sqrt": ("float r = 1.0f / sqrtf(mean + eps);", "float r = 1.0f / (sqrtf(mean) + eps);"),
+    "rms32_mean_over_h_minus_one": ("float mean = ss / (float)H;", "float mean = ss / (float)(H - 1);"),
+    "rms32_y_from_rounded_x": ("float t = x[h] * r;",
+                               "float t = oracle_bf16_to_f32(oracle_bf16_from_f32(x[h])) * r;"),
     "combine_shared_axes_transposed": (
         "acc = acc + oracle_bf16_to_f32(shared[((s * S + qq) * T + t) * H + h]);",
         "acc = acc + oracle_bf16_to_f32(shared[((qq * (int64_t)R + s) * T + t) * H + h]);"),
@@ -132,7 +139,10 @@ def pins():
               tnf.test_mx_all_subnormal_block, tnf.test_mx_block_maximum_skips_nan,
               tnf.test_mx_block_of_nan_only_takes_the_smallest_exponent]
     cases += [trn.test_hand_worked_row, lambda: trn.test_constant_row(1e-3, 1e-6),
-              lambda: trn.test_constant_row(0.75, 1e-6), lambda: trn.test_matches_torch_rms_norm_float64(1e-6)]
+              lambda: trn.test_constant_row(0.75, 1e-6), lambda: trn.test_matches_torch_rms_norm_float64(1e-6),
+              trn.test_f32_steps_hand_worked_exact,
+              lambda: trn.test_f32_steps_match_an_independent_float32_route(256, 1e-6),
+              lambda: trn.test_f32_steps_match_an_independent_float32_route(520, 0.5)]
     return cases
 
 

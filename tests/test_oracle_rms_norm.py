@@ -111,3 +111,66 @@ def test_tolerance_accepts_float32_steps_and_rejects_bf16_steps():
     # a residual left out is rejected
     ok, _ = oracle.add_rms_norm_within_tolerance(oracle.combine(lay, y_bits, wts), rs, yo, ref, w.K, 0)
     assert not ok
+
+
+def f32_route_from_c(c_bits, res_bits, g_bits, eps):
+    """numpy's binary32 operations, one step at a time (an independent route
+    through the same IEEE operations), from the combine's bf16 output."""
+    c = oracle.bf16_bits_to_f64(c_bits).astype(np.float32)
+    r = oracle.bf16_bits_to_f64(res_bits).astype(np.float32).reshape(c.shape)
+    x = (c + r).astype(np.float32)
+    ss = np.zeros(x.shape[0], np.float32)
+    for h in range(x.shape[1]):
+        ss = (ss + (x[:, h] * x[:, h]).astype(np.float32)).astype(np.float32)
+    mean = (ss / np.float32(x.shape[1])).astype(np.float32)
+    rstd = (np.float32(1.0) / np.sqrt((mean + np.float32(eps)).astype(np.float32))).astype(np.float32)
+    g = oracle.bf16_bits_to_f64(g_bits).astype(np.float32)
+    yv = ((x * rstd[:, None]).astype(np.float32) * g[None, :]).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    yb = torch.from_numpy(yv).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return xb, rstd, yb
+
+
+def test_f32_steps_hand_worked_exact():
+    # c = 1, r = 1: x = 2 everywhere; sum of squares 16, mean 4, sqrt 2, rstd 0.5;
+    # y = (2 * 0.5) * gamma = gamma; every step exact
+    H = 4
+    g = bits([1.0, -2.0, 0.75, 3.0])
+    x, rstd, y = oracle.add_rms_norm_f32(bits(np.ones((1, H))), bits(np.ones((1, H))), g, 0.0)
+    assert np.array_equal(x, bits(np.full((1, H), 2.0)))
+    assert rstd[0] == np.float32(0.5)
+    assert np.array_equal(y[0], g)
+    # with eps = 12: mean 4 + 12 = 16, rstd 0.25, y = gamma / 2
+    x, rstd, y = oracle.add_rms_norm_f32(bits(np.ones((1, H))), bits(np.ones((1, H))), g, 12.0)
+    assert rstd[0] == np.float32(0.25)
+    assert np.array_equal(y[0], bits(oracle.bf16_bits_to_f64(g) / 2))
+
+
+@pytest.mark.parametrize("H,eps", [(256, 1e-6), (7168, 1e-6), (520, 0.5)])
+def test_f32_steps_match_an_independent_float32_route(H, eps):
+    rng = np.random.default_rng(H)
+    N = 6
+    c = bits(rng.standard_normal((N, H)) * 2.0)
+    res = bits(rng.standard_normal((N, H)))
+    g = bits(1.0 + 0.1 * rng.standard_normal(H))
+    x, rstd, y = oracle.add_rms_norm_f32(c, res, g, eps)
+    xe, re, ye = f32_route_from_c(c, res, g, eps)
+    assert np.array_equal(x, xe)
+    assert np.array_equal(rstd.view(np.uint32), re.view(np.uint32))
+    assert np.array_equal(y, ye)
+
+
+def test_f32_steps_within_the_derived_bound_of_the_exact_result():
+    w = synth.WORKLOADS[1].with_(T=16, H=256)
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    lay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    y_bits, _ = oracle.dispatch(lay, synth.gen_x(w), 0)
+    y_bits = y_bits.view(np.uint16).reshape(-1, w.H)
+    res = synth.gen_residual(w)
+    g = synth.gen_gamma(w)
+    eps = synth.RMS_NORM_EPS
+    ref = oracle.combine_add_rms_norm_ref64(lay, y_bits, wts, None, res, g, eps)
+    xo, rs, yo = oracle.add_rms_norm_f32(oracle.combine(lay, y_bits, wts), res.reshape(-1, w.H), g, eps)
+    ok, worst = oracle.add_rms_norm_within_tolerance(xo, rs, yo, ref, w.K, 0)
+    assert ok, worst
