@@ -3,6 +3,8 @@
 // (E, H)): each valid entry (s, t, k) receives x[s, t] * scales[e] encoded by
 // the mode's rule, e = topk[s, t, k], so a token is encoded once per
 // destination rather than once per token.
+#include <cfloat>
+
 #include "quant.cuh"
 
 namespace {
@@ -10,6 +12,53 @@ namespace {
 #ifndef EP_EXPERT_SCALED_VPT
 #define EP_EXPERT_SCALED_VPT 4   // 16-byte vectors per thread in the per-expert-scale kernel
 #endif
+
+// max(a, b) that is NaN when either operand is NaN (PTX max.NaN): a row
+// maximum taken with it tells whether any product of the row is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+#ifndef EP_SCALED_PACKED
+#define EP_SCALED_PACKED 1
+#endif
+
+// max(a, b, c), NaN when any operand is NaN (three-operand PTX max).
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Two float32 products (or sums) in one packed instruction (PTX mul/add
+// .rn.f32x2), each rounded to nearest even like __fmul_rn / __fadd_rn.
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+    uint64_t x, y, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+}
+__device__ __forceinline__ void add2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+    uint64_t x, y, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+}
+
+// Round-to-nearest-even of v to an integer by one float32 addition: for
+// |v| < 2^22, fl(v + 1.5 * 2^23) lies in [2^23, 2^24), where the spacing of
+// float32 is 1, so the addition's own rounding (to nearest, ties to even;
+// 1.5 * 2^23 is even) yields 1.5 * 2^23 + rne(v), and the low byte of its
+// bits is rne(v) as a two's-complement int8 whenever |rne(v)| <= 128.  This
+// replaces a float-to-int conversion (a quarter-rate instruction) on the
+// per-expert int8 path, whose codes are all within +-127.
+__device__ __forceinline__ uint32_t rne_low_byte(float v) {
+    return __float_as_uint(__fadd_rn(v, 12582912.0f));
+}
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
@@ -31,6 +80,7 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
     // per-destination warp maxima, [destination][warp]; the slots of absent
     // warps stay 0 so that a destination's slots are read four at a time
     __shared__ __align__(16) uint32_t sred[kMaxTopk][32];
+    __shared__ uint32_t snan[32];   // per-warp maxima of the rare rows holding a NaN product
     const int total = a.expert_base[a.E];
     if ((int64_t)total > a.cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ep_set_status(a.status, EP_ERR_CAPACITY);
@@ -100,32 +150,54 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
             float f[VPT][8];
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
+#if EP_SCALED_PACKED
+                mul2_rn(xf[u][0], xf[u][1], sc[u][0].x, sc[u][0].y, f[u][0], f[u][1]);
+                mul2_rn(xf[u][2], xf[u][3], sc[u][0].z, sc[u][0].w, f[u][2], f[u][3]);
+                mul2_rn(xf[u][4], xf[u][5], sc[u][1].x, sc[u][1].y, f[u][4], f[u][5]);
+                mul2_rn(xf[u][6], xf[u][7], sc[u][1].z, sc[u][1].w, f[u][6], f[u][7]);
+#else
                 f[u][0] = __fmul_rn(xf[u][0], sc[u][0].x); f[u][1] = __fmul_rn(xf[u][1], sc[u][0].y);
                 f[u][2] = __fmul_rn(xf[u][2], sc[u][0].z); f[u][3] = __fmul_rn(xf[u][3], sc[u][0].w);
                 f[u][4] = __fmul_rn(xf[u][4], sc[u][1].x); f[u][5] = __fmul_rn(xf[u][5], sc[u][1].y);
                 f[u][6] = __fmul_rn(xf[u][6], sc[u][1].z); f[u][7] = __fmul_rn(xf[u][7], sc[u][1].w);
+#endif
             }
             if (j + 1 < nvd) load_scales(sc, sexp[j + 1]);   // overlaps the rest of this destination
             float s_tok = 0.0f, amax = 0.0f;
+            bool nan_row = false;
+            // int8: the row maximum propagates NaN, so one test shows whether
+            // the fast rounding below may be used (FP8 modes skip NaN at once)
+            constexpr bool kNanTrack = (Q == M_INT8);
             if constexpr (TR::token) {
                 // row maximum: a tree over the thread's elements, one warp
                 // reduction instruction, then the warps' slots
+                auto mx = [](float p, float q) { return kNanTrack ? fmax_nan(p, q) : fmaxf(p, q); };
                 float t[VPT];
 #pragma unroll
                 for (int u = 0; u < VPT; ++u) {
-                    const float a01 = fmaxf(fabsf(f[u][0]), fabsf(f[u][1]));
-                    const float a23 = fmaxf(fabsf(f[u][2]), fabsf(f[u][3]));
-                    const float a45 = fmaxf(fabsf(f[u][4]), fabsf(f[u][5]));
-                    const float a67 = fmaxf(fabsf(f[u][6]), fabsf(f[u][7]));
-                    t[u] = fmaxf(fmaxf(a01, a23), fmaxf(a45, a67));
+#if EP_SCALED_PACKED
+                    if constexpr (kNanTrack) {
+                        const float a = fmax3_nan(fabsf(f[u][0]), fabsf(f[u][1]), fabsf(f[u][2]));
+                        const float b = fmax3_nan(fabsf(f[u][3]), fabsf(f[u][4]), fabsf(f[u][5]));
+                        t[u] = fmax3_nan(a, b, fmax_nan(fabsf(f[u][6]), fabsf(f[u][7])));
+                        continue;
+                    }
+#endif
+                    const float a01 = mx(fabsf(f[u][0]), fabsf(f[u][1]));
+                    const float a23 = mx(fabsf(f[u][2]), fabsf(f[u][3]));
+                    const float a45 = mx(fabsf(f[u][4]), fabsf(f[u][5]));
+                    const float a67 = mx(fabsf(f[u][6]), fabsf(f[u][7]));
+                    t[u] = mx(mx(a01, a23), mx(a45, a67));
                 }
 #pragma unroll
                 for (int w2 = 1; w2 < VPT; w2 <<= 1)
 #pragma unroll
-                    for (int u = 0; u + w2 < VPT; u += 2 * w2) t[u] = fmaxf(t[u], t[u + w2]);
-                // fmaxf returns the other operand for one NaN and NaN for two:
-                // the 0 operand makes an all-NaN slice 0, like a running maximum
-                uint32_t m = __float_as_uint(fmaxf(0.0f, t[0]));
+                    for (int u = 0; u + w2 < VPT; u += 2 * w2) t[u] = mx(t[u], t[u + w2]);
+                // NaN tracking: a NaN's bits (0x7fffffff) order above every
+                // magnitude.  Otherwise fmaxf returns the other operand for one
+                // NaN and NaN for two: the 0 operand makes an all-NaN slice 0,
+                // like a running maximum.
+                uint32_t m = __float_as_uint(kNanTrack ? t[0] : fmaxf(0.0f, t[0]));
                 m = __reduce_max_sync(kFull, m);
                 if (lane == 0) sred[j][warp] = m;
                 __syncthreads();
@@ -135,27 +207,58 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                     const uint4 q4 = slots[i];
                     m = max(m, max(max(q4.x, q4.y), max(q4.z, q4.w)));
                 }
+                if (kNanTrack && m > 0x7f800000u) {
+                    // a NaN product (rare; the same m in every thread, so the
+                    // barrier is reached by all): the maximum that skips NaN
+                    nan_row = true;
+                    float t2 = 0.0f;
+#pragma unroll
+                    for (int u = 0; u < VPT; ++u)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) t2 = fmaxf(t2, fabsf(f[u][i]));
+                    const uint32_t m2 = __reduce_max_sync(kFull, __float_as_uint(t2));
+                    if (lane == 0) snan[warp] = m2;
+                    __syncthreads();
+                    m = 0;
+                    for (int i = 0; i < (NT >> 5); ++i) m = max(m, snan[i]);
+                }
                 amax = __uint_as_float(m);
                 s_tok = __fdiv_rn(TR::dmax, amax);
             }
-            // int8 with a finite scale: |fl(f * s)| <= 127 (1 + 2^-24) for every
-            // element, so the rounded code is within +-127 and the clamp is
-            // idle; a NaN product converts to 0.  Only an infinite scale (a
-            // row whose maximum is subnormal, or zero) needs the clamped form.
-            const bool no_clamp = (Q == M_INT8) && amax > 0.0f && !isinf(s_tok);
+            // int8 with a finite nonzero row maximum, a finite scale and no NaN
+            // product: every |fl(f * s)| <= 127 (1 + 2^-24), so every code is
+            // rne(fl(f * s)) within +-127 and one float32 addition rounds it.
+            // Otherwise (a NaN product, an infinite maximum, or an infinite
+            // scale from a zero or subnormal maximum) the clamped conversion,
+            // which also turns a NaN product into 0.
+            const bool fast = (Q == M_INT8) && !nan_row && amax > 0.0f && amax <= FLT_MAX && s_tok <= FLT_MAX;
             uint8_t* row = a.data + (int64_t)d * a.row_bytes;
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
                 uint32_t packed[2], sb = 0;
                 float gi = 0.0f;
-                if (no_clamp) {
+                if (fast) {
                     const float* g = f[u];
+#if EP_SCALED_PACKED
+                    constexpr float kRne = 12582912.0f;
+                    float v[8], r[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        mul2_rn(g[i], g[i + 1], s_tok, s_tok, v[i], v[i + 1]);
+                        add2_rn(v[i], v[i + 1], kRne, kRne, r[i], r[i + 1]);
+                    }
+                    packed[0] = pack4_low_bytes(__float_as_int(r[0]), __float_as_int(r[1]),
+                                                __float_as_int(r[2]), __float_as_int(r[3]));
+                    packed[1] = pack4_low_bytes(__float_as_int(r[4]), __float_as_int(r[5]),
+                                                __float_as_int(r[6]), __float_as_int(r[7]));
+#else
                     packed[0] = pack4_low_bytes(
-                        __float2int_rn(__fmul_rn(g[0], s_tok)), __float2int_rn(__fmul_rn(g[1], s_tok)),
-                        __float2int_rn(__fmul_rn(g[2], s_tok)), __float2int_rn(__fmul_rn(g[3], s_tok)));
+                        (int)rne_low_byte(__fmul_rn(g[0], s_tok)), (int)rne_low_byte(__fmul_rn(g[1], s_tok)),
+                        (int)rne_low_byte(__fmul_rn(g[2], s_tok)), (int)rne_low_byte(__fmul_rn(g[3], s_tok)));
                     packed[1] = pack4_low_bytes(
-                        __float2int_rn(__fmul_rn(g[4], s_tok)), __float2int_rn(__fmul_rn(g[5], s_tok)),
-                        __float2int_rn(__fmul_rn(g[6], s_tok)), __float2int_rn(__fmul_rn(g[7], s_tok)));
+                        (int)rne_low_byte(__fmul_rn(g[4], s_tok)), (int)rne_low_byte(__fmul_rn(g[5], s_tok)),
+                        (int)rne_low_byte(__fmul_rn(g[6], s_tok)), (int)rne_low_byte(__fmul_rn(g[7], s_tok)));
+#endif
                 } else {
                     // the raw vector is only read by the MX modes, which take no input scales
                     encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
