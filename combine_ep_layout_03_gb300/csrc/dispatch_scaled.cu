@@ -21,6 +21,11 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
     return r;
 }
 
+// Packed float32 products of x and the scale row (mul.rn.f32x2), and the
+// row maximum by three-operand max; the rounding of the codes stays scalar
+// (__fmul_rn then __fadd_rn): a packed multiply feeding a packed add gave
+// results that differ from two separately rounded operations in rare
+// elements, i.e. not the two roundings the encoding needs.
 #ifndef EP_SCALED_PACKED
 #define EP_SCALED_PACKED 1
 #endif
@@ -32,8 +37,8 @@ __device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
     return r;
 }
 
-// Two float32 products (or sums) in one packed instruction (PTX mul/add
-// .rn.f32x2), each rounded to nearest even like __fmul_rn / __fadd_rn.
+// Two float32 products in one packed instruction (PTX mul.rn.f32x2), each
+// rounded to nearest even like __fmul_rn.
 __device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
     uint64_t x, y, r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
@@ -41,14 +46,6 @@ __device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, 
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
 }
-__device__ __forceinline__ void add2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
-    uint64_t x, y, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
-}
-
 // Round-to-nearest-even of v to an integer by one float32 addition: for
 // |v| < 2^22, fl(v + 1.5 * 2^23) lies in [2^23, 2^24), where the spacing of
 // float32 is 1, so the addition's own rounding (to nearest, ties to even;
@@ -239,26 +236,12 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 float gi = 0.0f;
                 if (fast) {
                     const float* g = f[u];
-#if EP_SCALED_PACKED
-                    constexpr float kRne = 12582912.0f;
-                    float v[8], r[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        mul2_rn(g[i], g[i + 1], s_tok, s_tok, v[i], v[i + 1]);
-                        add2_rn(v[i], v[i + 1], kRne, kRne, r[i], r[i + 1]);
-                    }
-                    packed[0] = pack4_low_bytes(__float_as_int(r[0]), __float_as_int(r[1]),
-                                                __float_as_int(r[2]), __float_as_int(r[3]));
-                    packed[1] = pack4_low_bytes(__float_as_int(r[4]), __float_as_int(r[5]),
-                                                __float_as_int(r[6]), __float_as_int(r[7]));
-#else
                     packed[0] = pack4_low_bytes(
                         (int)rne_low_byte(__fmul_rn(g[0], s_tok)), (int)rne_low_byte(__fmul_rn(g[1], s_tok)),
                         (int)rne_low_byte(__fmul_rn(g[2], s_tok)), (int)rne_low_byte(__fmul_rn(g[3], s_tok)));
                     packed[1] = pack4_low_bytes(
                         (int)rne_low_byte(__fmul_rn(g[4], s_tok)), (int)rne_low_byte(__fmul_rn(g[5], s_tok)),
                         (int)rne_low_byte(__fmul_rn(g[6], s_tok)), (int)rne_low_byte(__fmul_rn(g[7], s_tok)));
-#endif
                 } else {
                     // the raw vector is only read by the MX modes, which take no input scales
                     encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
