@@ -263,7 +263,9 @@ def algorithmic_bytes(w, quant, rows, V, per_rank=False, fmt="", trows=0):
     disp = N * H * 2 + N * K * 4 + rows * (db + sb)
     if fmt == "pre":
         disp = N * (db + sb) + N * K * 4 + rows * (db + sb)
-    norm = N * H * 2 * 3 + H * 2 + N * 4 if fmt == "norm" else 0   # residual in; x, rstd out
+    # the combine's own output is y; the epilogue adds the residual read, the x
+    # output, gamma and rstd
+    norm = N * H * 2 * 2 + H * 2 + N * 4 if fmt == "norm" else 0
     if fmt == "split":
         # send: x in, arrival rows out; wait: V arrival rows in, grouped rows out
         disp = N * H * 2 + N * K * 4 + trows * (db + sb) + V * (db + sb) + rows * (db + sb) + rows * 4
