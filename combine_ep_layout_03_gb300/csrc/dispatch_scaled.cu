@@ -21,39 +21,22 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
     return r;
 }
 
-// Packed float32 products of x and the scale row (mul.rn.f32x2), and the
-// row maximum by three-operand max; the rounding of the codes stays scalar
-// (__fmul_rn then __fadd_rn): a packed multiply feeding a packed add gave
-// results that differ from two separately rounded operations in rare
-// elements, i.e. not the two roundings the encoding needs.
-#ifndef EP_SCALED_PACKED
-#define EP_SCALED_PACKED 1
-#endif
-// EP_SCALED_MAXABS: the int8 row maximum by three-operand max of magnitudes
-// (max.NaN.abs), no separate absolute values.  EP_SCALED_RECOMPUTE: the
-// products are computed again for the encoding instead of being kept across
-// the barrier, and the next scale slice is not prefetched, so fewer registers
-// are live (more CTAs per SM).  EP_SCALED_MAXNREG: register cap per thread
-// (0: the launch bound alone).
-#ifndef EP_SCALED_MAXABS
-#define EP_SCALED_MAXABS 0
-#endif
-#ifndef EP_SCALED_RECOMPUTE
-#define EP_SCALED_RECOMPUTE 0
-#endif
-#ifndef EP_SCALED_MAXNREG
-#define EP_SCALED_MAXNREG 0
-#endif
-
-// max(a, b, c), NaN when any operand is NaN (three-operand PTX max).
-__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+// max(|a|, |b|, |c|), NaN when any operand is NaN (three-operand PTX max of
+// magnitudes): the int8 row maximum in one instruction per three elements.
+__device__ __forceinline__ float fmax3_abs_nan(float a, float b, float c) {
     float r;
-    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 
 // Two float32 products in one packed instruction (PTX mul.rn.f32x2), each
-// rounded to nearest even like __fmul_rn.
+// rounded to nearest even like __fmul_rn.  The second form is the same
+// product as an instruction the compiler may not merge with an earlier
+// identical one, so that the first result need not stay live across the
+// barrier.  The codes' own rounding (a product, then the rounding addition
+// below) stays scalar: a packed multiply feeding a packed addition was
+// measured to differ, in rare elements, from two separately rounded
+// operations (it behaves as one fused, singly rounded operation).
 __device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
     uint64_t x, y, r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
@@ -61,15 +44,6 @@ __device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, 
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
 }
-// max(|a|, |b|, |c|), NaN when any operand is NaN.
-__device__ __forceinline__ float fmax3_abs_nan(float a, float b, float c) {
-    float r;
-    asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-// The packed product again, as an instruction the compiler may not merge
-// with an earlier identical one (so the first result need not stay live).
 __device__ __forceinline__ void mul2_rn_again(float a0, float a1, float b0, float b1, float& r0, float& r1) {
     uint64_t x, y, r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
@@ -89,23 +63,25 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
     return __float_as_uint(__fadd_rn(v, 12582912.0f));
 }
 
+// Register cap of the per-expert kernel: 72 registers let four CTAs of 224
+// threads share an SM (28 warps to hide the per-destination barrier and the
+// scale loads), at the cost of a few bytes of spill.
+#ifndef EP_SCALED_MAXNREG
+#define EP_SCALED_MAXNREG 72
+#endif
+
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
 // expert.  Warp 0 finds the experts of the valid destinations (bisection over
-// expert_base) and lists them compactly; each destination then takes one pass
-// over its scale-row slice (per-token modes add one CTA reduction of the row
-// maximum; each destination has its own reduction slot, so one barrier per
-// destination suffices) and every thread stores its codes directly.  The next
-// destination's scale slice is loaded into registers while the current one is
-// encoded, so its L2 latency overlaps the barrier and the stores.
+// expert_base) and lists them compactly; each destination then loads its
+// scale-row slice and forms the products (per-token modes add one CTA
+// reduction of the row maximum; each destination has its own reduction slot,
+// so one barrier per destination suffices), forms the products again after
+// the barrier rather than keeping them, and every thread stores its codes
+// directly.  Keeping neither the products nor a prefetched next slice live is
+// what brings the kernel to four CTAs per SM.
 template <int Q, int VPT>
-__global__ void
-#if EP_SCALED_MAXNREG > 0
-__maxnreg__(EP_SCALED_MAXNREG)
-#else
-__launch_bounds__(1024 / VPT)
-#endif
-dispatch_expert_scaled_kernel(DispatchArgs a) {
+__global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
     extern __shared__ int sbase[];   // [E+1] first row of each expert
     __shared__ int sdst[kMaxTopk];
@@ -182,7 +158,6 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
         auto products = [&](float (&f)[VPT][8], bool again) {
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
-#if EP_SCALED_PACKED
                 if (again) {
                     mul2_rn_again(xf[u][0], xf[u][1], sc[u][0].x, sc[u][0].y, f[u][0], f[u][1]);
                     mul2_rn_again(xf[u][2], xf[u][3], sc[u][0].z, sc[u][0].w, f[u][2], f[u][3]);
@@ -194,27 +169,13 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 mul2_rn(xf[u][2], xf[u][3], sc[u][0].z, sc[u][0].w, f[u][2], f[u][3]);
                 mul2_rn(xf[u][4], xf[u][5], sc[u][1].x, sc[u][1].y, f[u][4], f[u][5]);
                 mul2_rn(xf[u][6], xf[u][7], sc[u][1].z, sc[u][1].w, f[u][6], f[u][7]);
-#else
-                f[u][0] = __fmul_rn(xf[u][0], sc[u][0].x); f[u][1] = __fmul_rn(xf[u][1], sc[u][0].y);
-                f[u][2] = __fmul_rn(xf[u][2], sc[u][0].z); f[u][3] = __fmul_rn(xf[u][3], sc[u][0].w);
-                f[u][4] = __fmul_rn(xf[u][4], sc[u][1].x); f[u][5] = __fmul_rn(xf[u][5], sc[u][1].y);
-                f[u][6] = __fmul_rn(xf[u][6], sc[u][1].z); f[u][7] = __fmul_rn(xf[u][7], sc[u][1].w);
-#endif
             }
         };
-#if !EP_SCALED_RECOMPUTE
-        if (nvd > 0) load_scales(sc, sexp[0]);
-#endif
         for (int j = 0; j < nvd; ++j) {
             const int d = sdst[j];
             float f[VPT][8];
-#if EP_SCALED_RECOMPUTE
             load_scales(sc, sexp[j]);
             products(f, false);
-#else
-            products(f, false);
-            if (j + 1 < nvd) load_scales(sc, sexp[j + 1]);   // overlaps the rest of this destination
-#endif
             float s_tok = 0.0f, amax = 0.0f;
             bool nan_row = false;
             // int8: the row maximum propagates NaN, so one test shows whether
@@ -227,21 +188,12 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                 float t[VPT];
 #pragma unroll
                 for (int u = 0; u < VPT; ++u) {
-#if EP_SCALED_MAXABS
                     if constexpr (kNanTrack) {
                         const float a = fmax3_abs_nan(f[u][0], f[u][1], f[u][2]);
                         const float b = fmax3_abs_nan(f[u][3], f[u][4], f[u][5]);
                         t[u] = fmax3_abs_nan(a, b, fmax3_abs_nan(f[u][6], f[u][7], 0.0f));
                         continue;
                     }
-#elif EP_SCALED_PACKED
-                    if constexpr (kNanTrack) {
-                        const float a = fmax3_nan(fabsf(f[u][0]), fabsf(f[u][1]), fabsf(f[u][2]));
-                        const float b = fmax3_nan(fabsf(f[u][3]), fabsf(f[u][4]), fabsf(f[u][5]));
-                        t[u] = fmax3_nan(a, b, fmax_nan(fabsf(f[u][6]), fabsf(f[u][7])));
-                        continue;
-                    }
-#endif
                     const float a01 = mx(fabsf(f[u][0]), fabsf(f[u][1]));
                     const float a23 = mx(fabsf(f[u][2]), fabsf(f[u][3]));
                     const float a45 = mx(fabsf(f[u][4]), fabsf(f[u][5]));
@@ -266,9 +218,7 @@ dispatch_expert_scaled_kernel(DispatchArgs a) {
                     const uint4 q4 = slots[i];
                     m = max(m, max(max(q4.x, q4.y), max(q4.z, q4.w)));
                 }
-#if EP_SCALED_RECOMPUTE
                 products(f, true);   // f was not kept across the barrier
-#endif
                 if (kNanTrack && m > 0x7f800000u) {
                     // a NaN product (rare; the same m in every thread, so the
                     // barrier is reached by all): the maximum that skips NaN
