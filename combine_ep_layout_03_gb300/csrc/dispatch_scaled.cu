@@ -69,6 +69,9 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 #ifndef EP_SCALED_MAXNREG
 #define EP_SCALED_MAXNREG 72
 #endif
+#ifndef EP_SCALED_SCALAR_PRODUCTS
+#define EP_SCALED_SCALAR_PRODUCTS 0
+#endif
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
@@ -80,7 +83,7 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 // the barrier rather than keeping them, and every thread stores its codes
 // directly.  Keeping neither the products nor a prefetched next slice live is
 // what brings the kernel to four CTAs per SM.
-template <int Q, int VPT>
+template <int Q, int VPT, bool FULL>
 __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
     extern __shared__ int sbase[];   // [E+1] first row of each expert
@@ -108,7 +111,7 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
-            if (vi < a.nvec) {
+            if (FULL || vi < a.nvec) {
                 sc[u][0] = __ldg(srow + 2 * vi);
                 sc[u][1] = __ldg(srow + 2 * vi + 1);
             } else {
@@ -149,7 +152,7 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
-            unpack8(vi < a.nvec ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), xf[u]);
+            unpack8((FULL || vi < a.nvec) ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), xf[u]);
         }
         __syncthreads();
         const int nvd = snv;
@@ -158,6 +161,21 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
         auto products = [&](float (&f)[VPT][8], bool again) {
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
+#if EP_SCALED_SCALAR_PRODUCTS
+                const float s8[8] = {sc[u][0].x, sc[u][0].y, sc[u][0].z, sc[u][0].w,
+                                     sc[u][1].x, sc[u][1].y, sc[u][1].z, sc[u][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (again) {
+                        float r;
+                        asm volatile("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(xf[u][i]), "f"(s8[i]));
+                        f[u][i] = r;
+                    } else {
+                        f[u][i] = __fmul_rn(xf[u][i], s8[i]);
+                    }
+                }
+                continue;
+#endif
                 if (again) {
                     mul2_rn_again(xf[u][0], xf[u][1], sc[u][0].x, sc[u][0].y, f[u][0], f[u][1]);
                     mul2_rn_again(xf[u][2], xf[u][3], sc[u][0].z, sc[u][0].w, f[u][2], f[u][3]);
@@ -262,7 +280,7 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
                     encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
                 }
                 const int vi = u * NT + tid;
-                if (vi < a.nvec) {
+                if (FULL || vi < a.nvec) {
                     st_v2(row + (int64_t)vi * 8, make_uint2(packed[0], packed[1]));
                     if constexpr (TR::group) {
                         if ((vi & 15) == 0) *reinterpret_cast<float*>(scale_at(a, d, vi >> 4)) = gi;
@@ -282,15 +300,20 @@ cudaError_t launch_scaled_q(const ep_handle* h, const DispatchArgs& a, cudaStrea
     constexpr int EV = EP_EXPERT_SCALED_VPT;
     const int ent = ((a.nvec + EV - 1) / EV + 31) / 32 * 32;
     const size_t smem = sizeof(int) * (size_t)(a.E + 1);
+    // every thread's VPT vectors lie inside the row: no bounds checks
+    const bool full = (int64_t)ent * EV == a.nvec;
     int occ = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, dispatch_expert_scaled_kernel<Q, EV>, ent, smem);
+    cudaError_t err = full ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &occ, dispatch_expert_scaled_kernel<Q, EV, true>, ent, smem)
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &occ, dispatch_expert_scaled_kernel<Q, EV, false>, ent, smem);
     if (err != cudaSuccess) return err;
     const int64_t items = a.N + a.E;
     int64_t grid = (int64_t)h->num_sms * (occ > 0 ? occ : 1);
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
-    dispatch_expert_scaled_kernel<Q, EV><<<(unsigned)grid, ent, smem, st>>>(a);
+    if (full) dispatch_expert_scaled_kernel<Q, EV, true><<<(unsigned)grid, ent, smem, st>>>(a);
+    else dispatch_expert_scaled_kernel<Q, EV, false><<<(unsigned)grid, ent, smem, st>>>(a);
     return cudaGetLastError();
 }
 
