@@ -29,27 +29,13 @@ __device__ __forceinline__ float fmax3_abs_nan(float a, float b, float c) {
     return r;
 }
 
-// Two float32 products in one packed instruction (PTX mul.rn.f32x2), each
-// rounded to nearest even like __fmul_rn.  The second form is the same
-// product as an instruction the compiler may not merge with an earlier
-// identical one, so that the first result need not stay live across the
-// barrier.  The codes' own rounding (a product, then the rounding addition
-// below) stays scalar: a packed multiply feeding a packed addition was
-// measured to differ, in rare elements, from two separately rounded
-// operations (it behaves as one fused, singly rounded operation).
-__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
-    uint64_t x, y, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
-}
-__device__ __forceinline__ void mul2_rn_again(float a0, float a1, float b0, float b1, float& r0, float& r1) {
-    uint64_t x, y, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
-    asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+// A float32 product rounded to nearest even, as an instruction the compiler
+// may not merge with an earlier identical one: the products are formed again
+// after the barrier so that the first ones need not stay live across it.
+__device__ __forceinline__ float mul_rn_again(float a, float b) {
+    float r;
+    asm volatile("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
 }
 
 // Round-to-nearest-even of v to an integer by one float32 addition: for
@@ -68,9 +54,6 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 // scale loads), at the cost of a few bytes of spill.
 #ifndef EP_SCALED_MAXNREG
 #define EP_SCALED_MAXNREG 72
-#endif
-#ifndef EP_SCALED_SCALAR_PRODUCTS
-#define EP_SCALED_SCALAR_PRODUCTS 0
 #endif
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
@@ -161,32 +144,11 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
         auto products = [&](float (&f)[VPT][8], bool again) {
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
-#if EP_SCALED_SCALAR_PRODUCTS
                 const float s8[8] = {sc[u][0].x, sc[u][0].y, sc[u][0].z, sc[u][0].w,
                                      sc[u][1].x, sc[u][1].y, sc[u][1].z, sc[u][1].w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (again) {
-                        float r;
-                        asm volatile("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(xf[u][i]), "f"(s8[i]));
-                        f[u][i] = r;
-                    } else {
-                        f[u][i] = __fmul_rn(xf[u][i], s8[i]);
-                    }
-                }
-                continue;
-#endif
-                if (again) {
-                    mul2_rn_again(xf[u][0], xf[u][1], sc[u][0].x, sc[u][0].y, f[u][0], f[u][1]);
-                    mul2_rn_again(xf[u][2], xf[u][3], sc[u][0].z, sc[u][0].w, f[u][2], f[u][3]);
-                    mul2_rn_again(xf[u][4], xf[u][5], sc[u][1].x, sc[u][1].y, f[u][4], f[u][5]);
-                    mul2_rn_again(xf[u][6], xf[u][7], sc[u][1].z, sc[u][1].w, f[u][6], f[u][7]);
-                    continue;
-                }
-                mul2_rn(xf[u][0], xf[u][1], sc[u][0].x, sc[u][0].y, f[u][0], f[u][1]);
-                mul2_rn(xf[u][2], xf[u][3], sc[u][0].z, sc[u][0].w, f[u][2], f[u][3]);
-                mul2_rn(xf[u][4], xf[u][5], sc[u][1].x, sc[u][1].y, f[u][4], f[u][5]);
-                mul2_rn(xf[u][6], xf[u][7], sc[u][1].z, sc[u][1].w, f[u][6], f[u][7]);
+                for (int i = 0; i < 8; ++i)
+                    f[u][i] = again ? mul_rn_again(xf[u][i], s8[i]) : __fmul_rn(xf[u][i], s8[i]);
             }
         };
         for (int j = 0; j < nvd; ++j) {
