@@ -6,7 +6,6 @@
 #include <cfloat>
 
 #include "quant.cuh"
-#include "tma.cuh"
 
 namespace {
 
@@ -39,14 +38,6 @@ __device__ __forceinline__ float mul_rn_again(float a, float b) {
     return r;
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only; PTX cp.async.cg), the
-// issuing thread's own group; wait_group 0 makes the copies visible to it.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
 // Round-to-nearest-even of v to an integer by one float32 addition: for
 // |v| < 2^22, fl(v + 1.5 * 2^23) lies in [2^23, 2^24), where the spacing of
 // float32 is 1, so the addition's own rounding (to nearest, ties to even;
@@ -78,10 +69,7 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 template <int Q, int VPT, bool FULL>
 __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
-    // dynamic: [E+1] first row of each expert, then (16-byte aligned) the
-    // staging slots of the next scale slice, [VPT][2][NT] float4: each thread
-    // copies its own slice there a destination ahead and reads it back itself
-    extern __shared__ __align__(16) int sbase[];
+    extern __shared__ int sbase[];   // [E+1] first row of each expert
     __shared__ int sdst[kMaxTopk];
     __shared__ int sexp[kMaxTopk];
     __shared__ int snv;
@@ -100,30 +88,15 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
     for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
     for (int i = tid; i < kMaxTopk * 32; i += NT) (&sred[0][0])[i] = 0u;
     __syncthreads();
-    float4* stage = reinterpret_cast<float4*>(sbase + ((a.E + 1 + 3) & ~3));
-    // start the copy of this thread's scale slice of expert e (VPT x 2 float4)
-    // into its staging slots
-    auto stage_scales = [&](int e) {
+    // this thread's scale slice of expert e: VPT x 2 float4
+    auto load_scales = [&](float4 (&sc)[VPT][2], int e) {
         const float4* srow = reinterpret_cast<const float4*>(a.smooth + (int64_t)e * a.H);
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
             if (FULL || vi < a.nvec) {
-                cp_async16(stage + (2 * u) * NT + tid, srow + 2 * vi);
-                cp_async16(stage + (2 * u + 1) * NT + tid, srow + 2 * vi + 1);
-            }
-        }
-        cp_async_commit();
-    };
-    // wait for the staged slice and read it into registers
-    auto load_scales = [&](float4 (&sc)[VPT][2]) {
-        cp_async_wait_all();
-#pragma unroll
-        for (int u = 0; u < VPT; ++u) {
-            const int vi = u * NT + tid;
-            if (FULL || vi < a.nvec) {
-                sc[u][0] = stage[(2 * u) * NT + tid];
-                sc[u][1] = stage[(2 * u + 1) * NT + tid];
+                sc[u][0] = __ldg(srow + 2 * vi);
+                sc[u][1] = __ldg(srow + 2 * vi + 1);
             } else {
                 sc[u][0] = sc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -178,15 +151,11 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
                     f[u][i] = again ? mul_rn_again(xf[u][i], s8[i]) : __fmul_rn(xf[u][i], s8[i]);
             }
         };
-        if (nvd > 0) stage_scales(sexp[0]);
         for (int j = 0; j < nvd; ++j) {
             const int d = sdst[j];
             float f[VPT][8];
-            load_scales(sc);
+            load_scales(sc, sexp[j]);
             products(f, false);
-            // the slots are free once the products have consumed them: the
-            // next destination's slice travels during this one's work
-            if (j + 1 < nvd) stage_scales(sexp[j + 1]);
             float s_tok = 0.0f, amax = 0.0f;
             bool nan_row = false;
             // int8: the row maximum propagates NaN, so one test shows whether
@@ -292,7 +261,7 @@ template <int Q>
 cudaError_t launch_scaled_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     constexpr int EV = EP_EXPERT_SCALED_VPT;
     const int ent = ((a.nvec + EV - 1) / EV + 31) / 32 * 32;
-    const size_t smem = sizeof(int) * (size_t)((a.E + 1 + 3) & ~3) + sizeof(float4) * 2 * EV * (size_t)ent;
+    const size_t smem = sizeof(int) * (size_t)(a.E + 1);
     // every thread's VPT vectors lie inside the row: no bounds checks
     const bool full = (int64_t)ent * EV == a.nvec;
     int occ = 0;
