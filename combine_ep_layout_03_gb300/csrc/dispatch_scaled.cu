@@ -38,17 +38,6 @@ __device__ __forceinline__ float mul_rn_again(float a, float b) {
     return r;
 }
 
-// 16-byte read-only load kept in program order with the other volatile
-// statements (the products formed again): the next destination's scale
-// vector u is requested right after vector u's last use, not hoisted ahead
-// of it, so both slices are never live at once.
-__device__ __forceinline__ float4 ld_nc_f4_ordered(const float4* p) {
-    float4 v;
-    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-    return v;
-}
-
 // Round-to-nearest-even of v to an integer by one float32 addition: for
 // |v| < 2^22, fl(v + 1.5 * 2^23) lies in [2^23, 2^24), where the spacing of
 // float32 is 1, so the addition's own rounding (to nearest, ties to even;
@@ -66,9 +55,6 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 #ifndef EP_SCALED_MAXNREG
 #define EP_SCALED_MAXNREG 72
 #endif
-#ifndef EP_SCALED_ORDERED_LOADS
-#define EP_SCALED_ORDERED_LOADS 1
-#endif
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
@@ -83,11 +69,7 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 template <int Q, int VPT, bool FULL>
 __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
-    // dynamic: [E+1] first row of each expert, then (16-byte aligned) the
-    // token's row as float32, [2 * VPT][NT] float4: each thread keeps its own
-    // vectors there (written and read by that thread only) instead of in
-    // registers, which leaves room for the scale slice to be reloaded early
-    extern __shared__ __align__(16) int sbase[];
+    extern __shared__ int sbase[];   // [E+1] first row of each expert
     __shared__ int sdst[kMaxTopk];
     __shared__ int sexp[kMaxTopk];
     __shared__ int snv;
@@ -106,23 +88,20 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
     for (int e = tid; e <= a.E; e += NT) sbase[e] = a.expert_base[e];
     for (int i = tid; i < kMaxTopk * 32; i += NT) (&sred[0][0])[i] = 0u;
     __syncthreads();
-    // vector u of this thread's scale slice of expert e (two float4)
-    auto load_scale_vec = [&](float4 (&v)[2], int e, int u) {
+    // this thread's scale slice of expert e: VPT x 2 float4
+    auto load_scales = [&](float4 (&sc)[VPT][2], int e) {
         const float4* srow = reinterpret_cast<const float4*>(a.smooth + (int64_t)e * a.H);
-        const int vi = u * NT + tid;
-        if (FULL || vi < a.nvec) {
-#if EP_SCALED_ORDERED_LOADS
-            v[0] = ld_nc_f4_ordered(srow + 2 * vi);
-            v[1] = ld_nc_f4_ordered(srow + 2 * vi + 1);
-#else
-            v[0] = __ldg(srow + 2 * vi);
-            v[1] = __ldg(srow + 2 * vi + 1);
-#endif
-        } else {
-            v[0] = v[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const int vi = u * NT + tid;
+            if (FULL || vi < a.nvec) {
+                sc[u][0] = __ldg(srow + 2 * vi);
+                sc[u][1] = __ldg(srow + 2 * vi + 1);
+            } else {
+                sc[u][0] = sc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     };
-    float4* xs = reinterpret_cast<float4*>(sbase + ((a.E + 1 + 3) & ~3));
     const int64_t items = a.N + a.E;
     for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
         if (w >= a.N) {
@@ -152,39 +131,31 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
             if (lane == 0) snv = __popc(valid);
         }
         const uint16_t* xrow = a.x + w * a.H;
+        float xf[VPT][8];   // the row as floats, unpacked once for all destinations
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
-            // the row as floats, unpacked once for all destinations
             const int vi = u * NT + tid;
-            float t8[8];
-            unpack8((FULL || vi < a.nvec) ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), t8);
-            xs[(2 * u) * NT + tid] = make_float4(t8[0], t8[1], t8[2], t8[3]);
-            xs[(2 * u + 1) * NT + tid] = make_float4(t8[4], t8[5], t8[6], t8[7]);
+            unpack8((FULL || vi < a.nvec) ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), xf[u]);
         }
         __syncthreads();
         const int nvd = snv;
-        float4 sc[VPT][2];   // the current destination's scale slice
-        // product of x vector u and scale vector u, element by element (each
-        // rounded once); `again` forms it as an instruction the compiler may
-        // not merge with the first, so the first need not stay live
-        auto product_vec = [&](float (&g)[8], int u, bool again) {
-            const float4 x0 = xs[(2 * u) * NT + tid], x1 = xs[(2 * u + 1) * NT + tid];
-            const float x8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float s8[8] = {sc[u][0].x, sc[u][0].y, sc[u][0].z, sc[u][0].w,
-                                 sc[u][1].x, sc[u][1].y, sc[u][1].z, sc[u][1].w};
+        float4 sc[VPT][2];
+        // x * scale row, element by element (each product rounded once)
+        auto products = [&](float (&f)[VPT][8], bool again) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                g[i] = again ? mul_rn_again(x8[i], s8[i]) : __fmul_rn(x8[i], s8[i]);
+            for (int u = 0; u < VPT; ++u) {
+                const float s8[8] = {sc[u][0].x, sc[u][0].y, sc[u][0].z, sc[u][0].w,
+                                     sc[u][1].x, sc[u][1].y, sc[u][1].z, sc[u][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    f[u][i] = again ? mul_rn_again(xf[u][i], s8[i]) : __fmul_rn(xf[u][i], s8[i]);
+            }
         };
-        if (nvd > 0) {
-#pragma unroll
-            for (int u = 0; u < VPT; ++u) load_scale_vec(sc[u], sexp[0], u);
-        }
         for (int j = 0; j < nvd; ++j) {
             const int d = sdst[j];
             float f[VPT][8];
-#pragma unroll
-            for (int u = 0; u < VPT; ++u) product_vec(f[u], u, false);
+            load_scales(sc, sexp[j]);
+            products(f, false);
             float s_tok = 0.0f, amax = 0.0f;
             bool nan_row = false;
             // int8: the row maximum propagates NaN, so one test shows whether
@@ -227,18 +198,16 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
                     const uint4 q4 = slots[i];
                     m = max(m, max(max(q4.x, q4.y), max(q4.z, q4.w)));
                 }
+                products(f, true);   // f was not kept across the barrier
                 if (kNanTrack && m > 0x7f800000u) {
                     // a NaN product (rare; the same m in every thread, so the
                     // barrier is reached by all): the maximum that skips NaN
                     nan_row = true;
                     float t2 = 0.0f;
 #pragma unroll
-                    for (int u = 0; u < VPT; ++u) {
-                        float g[8];
-                        product_vec(g, u, true);
+                    for (int u = 0; u < VPT; ++u)
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) t2 = fmaxf(t2, fabsf(g[i]));
-                    }
+                        for (int i = 0; i < 8; ++i) t2 = fmaxf(t2, fabsf(f[u][i]));
                     const uint32_t m2 = __reduce_max_sync(kFull, __float_as_uint(t2));
                     if (lane == 0) snan[warp] = m2;
                     __syncthreads();
@@ -258,15 +227,10 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
             uint8_t* row = a.data + (int64_t)d * a.row_bytes;
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
-                // the products again, vector by vector; each scale vector is
-                // then free and takes the next destination's, whose load
-                // travels while this destination is encoded and stored
-                float g[8];
-                product_vec(g, u, true);
-                if (j + 1 < nvd) load_scale_vec(sc[u], sexp[j + 1], u);
                 uint32_t packed[2], sb = 0;
                 float gi = 0.0f;
                 if (fast) {
+                    const float* g = f[u];
                     packed[0] = pack4_low_bytes(
                         (int)rne_low_byte(__fmul_rn(g[0], s_tok)), (int)rne_low_byte(__fmul_rn(g[1], s_tok)),
                         (int)rne_low_byte(__fmul_rn(g[2], s_tok)), (int)rne_low_byte(__fmul_rn(g[3], s_tok)));
@@ -275,7 +239,7 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
                         (int)rne_low_byte(__fmul_rn(g[6], s_tok)), (int)rne_low_byte(__fmul_rn(g[7], s_tok)));
                 } else {
                     // the raw vector is only read by the MX modes, which take no input scales
-                    encode_vec<Q>(make_uint4(0, 0, 0, 0), g, s_tok, amax > 0.0f, packed, sb, gi);
+                    encode_vec<Q>(make_uint4(0, 0, 0, 0), f[u], s_tok, amax > 0.0f, packed, sb, gi);
                 }
                 const int vi = u * NT + tid;
                 if (FULL || vi < a.nvec) {
@@ -297,7 +261,7 @@ template <int Q>
 cudaError_t launch_scaled_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     constexpr int EV = EP_EXPERT_SCALED_VPT;
     const int ent = ((a.nvec + EV - 1) / EV + 31) / 32 * 32;
-    const size_t smem = sizeof(int) * (size_t)((a.E + 1 + 3) & ~3) + sizeof(float4) * 2 * EV * (size_t)ent;
+    const size_t smem = sizeof(int) * (size_t)(a.E + 1);
     // every thread's VPT vectors lie inside the row: no bounds checks
     const bool full = (int64_t)ent * EV == a.nvec;
     int occ = 0;
