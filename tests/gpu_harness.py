@@ -2,6 +2,9 @@
 on seeded inputs, and compare with the CPU oracle."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -109,3 +112,21 @@ def oracle_combine_sampled(olay, x_bits, wts, shared_tok, quant, mark_mod, token
         refs.append(r)
         mags.append(m)
     return np.concatenate(outs), np.concatenate(refs), np.concatenate(mags)
+
+
+def host_threads(cap: int = 16) -> int:
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    return max(1, min(cap, n))
+
+
+def for_row_chunks(total: int, fn, step: int = 32768, threads: int | None = None):
+    """Run fn(a, b) over [0, total) in chunks of `step` rows on host threads
+    (the oracle's C calls release the interpreter lock); re-raises the first
+    failure."""
+    if total <= 0:
+        return
+    with ThreadPoolExecutor(max_workers=threads or host_threads()) as ex:
+        list(ex.map(lambda a: fn(a, min(total, a + step)), range(0, total, step)))

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import to_dev_bf16
+from gpu_harness import for_row_chunks, host_threads, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -215,9 +215,9 @@ def test_edge_cases():
 
 
 def test_full_size_mxfp8_pre_encoded_and_block_major():
+    """Workload 4 at full size, the bench's keys 4p and 4x: every row."""
     w = synth.WORKLOADS[4]
     q = ep.EP_QUANT_MXFP8_E4M3
-    rng = np.random.default_rng(44)
     topk = synth.gen_topk(w)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
     lay, _, rows = expert_layout(w, topk)
@@ -229,27 +229,28 @@ def test_full_size_mxfp8_pre_encoded_and_block_major():
     scales.fill_(0xA5)
     lay.dispatch_ex(src_d, q, data, scales, x_scales=src_s, pre_encoded=True, block_major=True)
     assert lay.status() == ep.EP_OK
-    sample = np.unique(np.concatenate([rng.integers(0, rows, 3000), [0, rows - 1]])).astype(np.int64)
-    src = olay.recv_src[sample]
-    ridx = torch.from_numpy(sample).cuda()
-    got_d = data[ridx].cpu().numpy()
-    got_s = scales[:, ridx].cpu().numpy().T
+    # every receive row and scale column against the oracle's byte scatter of
+    # the pre-encoded source rows (padding rows zero), in chunks of rows
     sd, ss = src_d.cpu().numpy(), src_s.cpu().numpy()
-    valid = src >= 0
-    assert np.array_equal(got_d[valid], sd[src[valid]])
-    assert np.array_equal(got_s[valid], ss[src[valid]])
-    assert not got_d[~valid].any() and not got_s[~valid].any()
-    # padding rows (recv_src = -1) everywhere: data and scale columns zero
-    pad = torch.from_numpy(np.nonzero(olay.recv_src < 0)[0]).cuda()
-    assert not torch.any(data[pad]) and not torch.any(scales[:, pad])
 
-    # the fused MXFP8 dispatch writing block-major scales: the same columns as
-    # the oracle's row-major scales of the sampled rows
+    def check_pre(a, b):
+        assert np.array_equal(data[a:b].cpu().numpy(), oracle.dispatch_bytes(olay, sd, rows=b, row_begin=a))
+        assert np.array_equal(scales[:, a:b].cpu().numpy().T, oracle.dispatch_bytes(olay, ss, rows=b, row_begin=a))
+
+    for_row_chunks(rows, check_pre)
+
+    # the fused MXFP8 dispatch writing block-major scales: every row, and every
+    # column against the oracle's row-major scales
     x_dev = synth.gen_x_device(w)
     x = x_dev.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.N, w.H)
     scales.fill_(0xA5)
     lay.dispatch_ex(x_dev, q, data, scales, block_major=True)
     assert lay.status() == ep.EP_OK
-    od, os_ = oracle.dispatch_rows(olay, x, q, sample)
-    assert np.array_equal(data[ridx].cpu().numpy(), od)
-    assert np.array_equal(scales[:, ridx].cpu().numpy().T, os_)
+    enc_d, enc_s = oracle.encode_rows(q, x, host_threads())
+
+    def check_fused(a, b):
+        assert np.array_equal(data[a:b].cpu().numpy(), oracle.dispatch_bytes(olay, enc_d, rows=b, row_begin=a))
+        assert np.array_equal(scales[:, a:b].cpu().numpy().T,
+                              oracle.dispatch_bytes(olay, enc_s, rows=b, row_begin=a))
+
+    for_row_chunks(rows, check_fused)

@@ -162,3 +162,40 @@ def test_full_size(idx):
         out = g.combine(y, wts_dev, sh_dev)
         check_closed_form(w, topk, x_dev, wts_dev, sh_dev, out)
         assert g.lay.status() == 0
+
+
+def test_full_size_active_mask():
+    """Workload 5 at full size with a 2-D xActiveMask (the bench's key 5m): the
+    masked layout, every receive row and every combine output against the
+    oracle (masked entries take no part, like -1 ids)."""
+    from combine_ep_layout_03_gb300 import ep
+    w = synth.WORKLOADS[5]
+    topk = synth.gen_topk(w)
+    wts = synth.gen_weights(w, topk)
+    mask = synth.gen_mask(w, 2)
+    olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk, mask=mask)
+    lay = ep.EPLayout(w.R, w.T, w.H, w.E, w.K, w.alpha)
+    lay.layout(torch.from_numpy(topk).cuda(), active_mask=torch.from_numpy(mask).cuda())
+    v = {k: t.cpu().numpy() for k, t in lay.views().items()}
+    v["recv_src"] = v["recv_src"][: olay.rows]
+    compare_layout(v, olay)
+    assert lay.status() == 0
+    x_dev = synth.gen_x_device(w)
+    x = bf16_bits(x_dev).reshape(w.N, w.H)
+    sh_dev = synth.gen_shared_device(w)
+    enc_d, enc_s = oracle.encode_rows(0, x, host_threads(cap=64))
+    data, _ = lay.alloc_recv(0, max(olay.rows, 1))
+    data.fill_(0xA5)
+    lay.dispatch(x_dev, 0, data, None)
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    check_dispatch(olay, 0, w.H, data, None, enc_d, enc_s)
+    y = data.view(torch.bfloat16).view(-1, w.H)
+    lay.expert_identity(0, data, None, y, MARK)
+    # masked entries carry no weight, as in the benchmark
+    wm = np.where(mask.reshape(wts.shape) != 0, wts, np.float32(0)).astype(np.float32)
+    out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device="cuda")
+    lay.combine(y, torch.from_numpy(wm).cuda(), out, sh_dev)
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    check_combine(w, olay, 0, enc_d, enc_s, wm, sh_dev, out)

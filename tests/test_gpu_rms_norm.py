@@ -22,7 +22,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import GpuPath, bf16_bits, oracle_combine_sampled, to_dev_bf16
+from gpu_harness import GpuPath, bf16_bits, for_row_chunks, host_threads, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -129,9 +129,12 @@ def test_edges():
     assert torch.all(out == 3.0)
 
 
-def test_full_size_workload2_sampled():
+def test_full_size_workload2_every_token():
+    """Workload 2 at full size with the epilogue (the bench's key 2n): every
+    token's x_out, rstd and y within the derived bound of the oracle's float64
+    result, and against the oracle's float32 steps (bit-exact x_out where the
+    combines agree), in chunks of tokens on host threads."""
     w = synth.WORKLOADS[2]
-    rng = np.random.default_rng(12)
     topk = synth.gen_topk(w)
     wts = synth.gen_weights(w, topk)
     olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
@@ -145,20 +148,31 @@ def test_full_size_workload2_sampled():
     out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device="cuda")
     x_out = torch.empty_like(out)
     rstd = torch.empty(w.N, dtype=torch.float32, device="cuda")
-    g.lay.combine_add_rms_norm(y, torch.from_numpy(wts).cuda(), res_dev, to_dev_bf16(gam), out, x_out, rstd,
-                               None, EPS)
+    wts_dev = torch.from_numpy(wts).cuda()
+    g.lay.combine_add_rms_norm(y, wts_dev, res_dev, to_dev_bf16(gam), out, x_out, rstd, None, EPS)
+    c_gpu = bf16_bits(g.combine(y, wts_dev)).reshape(w.N, w.H)
+    torch.cuda.synchronize()
     assert g.lay.status() == ep.EP_OK
-    tokens = np.unique(np.concatenate([rng.integers(0, w.N, 300), [0, w.N - 1]]))
-    _, c, mag = oracle_combine_sampled(olay, x, wts, None, 0, 0, tokens)
-    tk = torch.from_numpy(tokens).cuda()
-    xr, rs, yv = oracle.add_rms_norm_ref64(c, bf16_bits(res_dev[tk]), gam, EPS)
-    ref = dict(c=c, mag=mag, x=xr, rstd=rs, y=yv, gamma=oracle.bf16_bits_to_f64(gam))
-    ok, worst = oracle.add_rms_norm_within_tolerance(bf16_bits(x_out[tk]), rstd[tk].cpu().numpy(),
-                                                     bf16_bits(out[tk]), ref, w.K, 0)
-    assert ok, worst
-    # float32 steps of the oracle on the sampled tokens
-    c_gpu = g.combine(y, torch.from_numpy(wts).cuda())
-    c_or, _, _ = oracle_combine_sampled(olay, x, wts, None, 0, 0, tokens)
-    xo, ro, yo = oracle.add_rms_norm_f32(c_or, bf16_bits(res_dev[tk]), gam, EPS)
-    check_against_f32_steps(bf16_bits(c_gpu[tk]), c_or, bf16_bits(x_out[tk]), xo, rstd[tk].cpu().numpy(), ro,
-                            bf16_bits(out[tk]), yo, w.H)
+    res = bf16_bits(res_dev).reshape(w.N, w.H)
+    xo_g, y_g, r_g = bf16_bits(x_out).reshape(w.N, w.H), bf16_bits(out).reshape(w.N, w.H), rstd.cpu().numpy()
+    dr = olay.dst_row.reshape(w.N, w.K)
+    wf = wts.reshape(w.N, w.K)
+
+    def chunk(a, b):
+        d = dr[a:b]
+        rows = np.unique(d[d >= 0]).astype(np.int64)
+        ymap = np.full(max(olay.rows, 1), -1, np.int64)
+        ymap[rows] = np.arange(len(rows))
+        od, _ = oracle.dispatch_rows(olay, x, 0, rows)   # identity experts: y = the receive rows
+        yo = od.view(np.uint16).reshape(len(rows), w.H)
+        mini = oracle.Layout(R=1, T=b - a, K=w.K, dst_row=np.ascontiguousarray(d.reshape(1, b - a, w.K)))
+        c, mag = oracle.combine_ref64(mini, yo, wf[a:b], None, 0, b - a, ymap)
+        xr, rs, yv = oracle.add_rms_norm_ref64(c, res[a:b], gam, EPS)
+        ref = dict(c=c, mag=mag, x=xr, rstd=rs, y=yv, gamma=oracle.bf16_bits_to_f64(gam))
+        ok, worst = oracle.add_rms_norm_within_tolerance(xo_g[a:b], r_g[a:b], y_g[a:b], ref, w.K, 0)
+        assert ok, (a, worst)
+        c_or = oracle.combine(mini, yo, wf[a:b], None, 0, b - a, ymap)
+        xo, ro, yo32 = oracle.add_rms_norm_f32(c_or, res[a:b], gam, EPS)
+        check_against_f32_steps(c_gpu[a:b], c_or, xo_g[a:b], xo, r_g[a:b], ro, y_g[a:b], yo32, w.H)
+
+    for_row_chunks(w.N, chunk, step=1024, threads=host_threads(cap=12))

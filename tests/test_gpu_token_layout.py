@@ -7,6 +7,8 @@ recv_topk_weights, receive rows and scales, the per-rank stand-in expert
 stage, and the reduced weights (both sum in ascending rank order).  Combine:
 within the derived tolerance.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -82,9 +84,15 @@ def test_token_layout_edges():
     run_tokens(synth.Workload(33, R=4, T=40, H=128, E=16, K=4, alpha=1, drop_p=0.6))
 
 
-def test_token_layout_full_size_workload2_sampled():
-    w = synth.WORKLOADS[2]
-    rng = np.random.default_rng(2)
+@pytest.mark.parametrize("idx,q", [(2, 0), (4, 4)])
+def test_token_layout_full_size_every_row(idx, q):
+    """Workloads 2 (bf16) and 4 (MXFP8 e4m3) at full size in the per-rank layout
+    (the bench's keys 2r and 4r): the layout arrays, recv_topk_idx /
+    recv_topk_weights and the reduced weights for every token, and every
+    receive row and scale row, in chunks of rows on host threads, against the
+    oracle's per-token encoding placed by its own tok_dst."""
+    from concurrent.futures import ThreadPoolExecutor
+    w = synth.WORKLOADS[idx]
     topk = synth.gen_topk(w)
     wts = synth.gen_weights(w, topk)
     tl = oracle.token_layout(w.R, w.T, w.E, w.K, topk, wts)
@@ -95,12 +103,39 @@ def test_token_layout_full_size_workload2_sampled():
     assert lay.token_rows()[-1] == tl.rows
     v = lay.views()
     assert np.array_equal(v["tok_dst"].cpu().numpy().reshape(w.N, w.K), tl.tok_dst)
+    assert np.array_equal(v["rank_tok_base"].cpu().numpy(), tl.rank_tok_base)
+    assert np.array_equal(v["recv_src_tok"][: tl.rows].cpu().numpy(), tl.recv_src)
     assert np.array_equal(ridx[: tl.rows].cpu().numpy(), tl.recv_topk_idx)
+    assert np.array_equal(rw[: tl.rows].cpu().numpy(), tl.recv_topk_weights)
     x_dev = synth.gen_x_device(w)
     x = bf16_bits(x_dev).reshape(w.N, w.H)
-    data, sc = lay.alloc_recv(0, tl.rows)
-    lay.dispatch_tokens(x_dev, 0, data, sc)
-    rows = np.unique(rng.integers(0, tl.rows, 2000))
-    got = data[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16)
-    assert np.array_equal(got, x[tl.recv_src[rows]])
+    data, sc = lay.alloc_recv(q, tl.rows)
+    data.fill_(0x3C)
+    if sc is not None:
+        sc.fill_(0x3C)
+    lay.dispatch_tokens(x_dev, q, data, sc)
+    torch.cuda.synchronize()
     assert lay.status() == 0
+    threads = max(1, min(16, len(os.sched_getaffinity(0))))
+    enc_d, enc_s = oracle.encode_rows(q, x, threads)
+    step = 32768
+
+    def chunk(a):
+        b = min(tl.rows, a + step)
+        od = oracle.dispatch_bytes(tl, enc_d, rows=b, row_begin=a)
+        assert np.array_equal(data[a:b].cpu().numpy(), od), f"receive rows {a}:{b} differ"
+        if sc is not None:
+            os_ = oracle.dispatch_bytes(tl, enc_s, rows=b, row_begin=a)
+            assert np.array_equal(sc[a:b].cpu().numpy(), os_), f"receive scales {a}:{b} differ"
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(chunk, range(0, tl.rows, step)))
+    # the per-rank expert stage and the combine with the reduced weights of every token
+    y = torch.empty((tl.rows, w.H), dtype=torch.bfloat16, device="cuda")
+    lay.expert_identity_tokens(q, data, sc, ridx, rw, y, 4)
+    out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device="cuda")
+    out_w = torch.empty((w.N, w.K), dtype=torch.float32, device="cuda")
+    lay.combine_tokens(y, out, None, rank_weights=rw, out_weights=out_w)
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    assert np.array_equal(out_w.cpu().numpy(), oracle.reduce_token_weights(tl, tl.recv_topk_weights))

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import bf16_bits, to_dev_bf16
+from gpu_harness import bf16_bits, for_row_chunks, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -124,7 +124,14 @@ def test_edges():
     assert torch.all(data == 9)
 
 
+def _same(dev_rows, expected):
+    assert np.array_equal(dev_rows.cpu().numpy(), expected)
+
+
 def test_full_size_workload2_two_phase_equals_one_call():
+    """Workload 2 at full size in the two-phase form (the bench's key 2a): every
+    arrival row and grouped row against the oracle, and both phases' results
+    equal to the one-call dispatch and combine bit for bit."""
     w = synth.WORKLOADS[2]
     topk = synth.gen_topk(w)
     wts = synth.gen_weights(w, topk)
@@ -139,6 +146,14 @@ def test_full_size_workload2_two_phase_equals_one_call():
     lay.dispatch_async(x_d, 0, td, None)
     data, _ = lay.alloc_recv(0, rows)
     lay.dispatch_wait(0, td, None, data, None)
+    torch.cuda.synchronize()
+    # every arrival row (per-rank layout) and every grouped row against the oracle
+    olay = oracle.layout(w.R, w.T, w.E, w.K, w.alpha, topk)
+    tl = oracle.token_layout(w.R, w.T, w.E, w.K, topk, wts)
+    assert olay.rows == rows and tl.rows == trows
+    xb = np.ascontiguousarray(x_d.view(torch.int16).cpu().numpy()).view(np.uint8).reshape(w.N, -1)
+    for_row_chunks(trows, lambda a, b: _same(td[a:b], oracle.dispatch_bytes(tl, xb, rows=b, row_begin=a)))
+    for_row_chunks(rows, lambda a, b: _same(data[a:b], oracle.dispatch_bytes(olay, xb, rows=b, row_begin=a)))
     del td
     ref, _ = lay.alloc_recv(0, rows)
     lay.dispatch(x_d, 0, ref, None)
