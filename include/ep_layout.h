@@ -239,8 +239,10 @@ ep_status ep_handle_status(const ep_handle* handle, ep_stream_t stream);
  * are 0 and the scale word is +inf.  A row whose maximum is subnormal
  * overflows s to +inf, so its codes are +-127 and 0 and the scale word is 0.
  * A NaN product converts to int8 code 0.  An MX block holding +-inf takes
- * sharedExp = 128 - emax and saturates the infinities.  The FP8/MX codes of a
- * NaN element are unspecified.
+ * sharedExp = 128 - emax and saturates the infinities.  The MX block maximum
+ * skips NaN elements too, so a block's scale byte and the codes of its other
+ * elements come from its non-NaN elements (a block of NaN only takes
+ * sharedExp = -127).  The FP8/MX codes of a NaN element are unspecified.
  * Padding rows get all-zero data and scale bytes.  recv_data holds
  * recv_rows_capacity rows of ep_recv_row_bytes().data_bytes; recv_scales
  * holds as many rows of scale_bytes (NULL for NONE).  If the layout needs more
