@@ -55,9 +55,6 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 #ifndef EP_SCALED_MAXNREG
 #define EP_SCALED_MAXNREG 72
 #endif
-#ifndef EP_SCALED_X_SMEM
-#define EP_SCALED_X_SMEM 0
-#endif
 
 // Per-expert input scales (EP_SCALES_PER_EXPERT, quantModes 1-3): the token is
 // encoded once per destination with the scale row of that destination's
@@ -72,9 +69,7 @@ __device__ __forceinline__ uint32_t rne_low_byte(float v) {
 template <int Q, int VPT, bool FULL>
 __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(DispatchArgs a) {
     using TR = QTraits<Q>;
-    // dynamic: [E+1] first row of each expert (then, 16-byte aligned, the
-    // row's float32 slots when the row is kept in shared memory)
-    extern __shared__ __align__(16) int sbase[];
+    extern __shared__ int sbase[];   // [E+1] first row of each expert
     __shared__ int sdst[kMaxTopk];
     __shared__ int sexp[kMaxTopk];
     __shared__ int snv;
@@ -136,25 +131,12 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
             if (lane == 0) snv = __popc(valid);
         }
         const uint16_t* xrow = a.x + w * a.H;
-#if EP_SCALED_X_SMEM
-        // the row as floats in the thread's own shared-memory slots
-        float4* xs = reinterpret_cast<float4*>(sbase + ((a.E + 1 + 3) & ~3));
-#pragma unroll
-        for (int u = 0; u < VPT; ++u) {
-            const int vi = u * NT + tid;
-            float t8[8];
-            unpack8((FULL || vi < a.nvec) ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), t8);
-            xs[(2 * u) * NT + tid] = make_float4(t8[0], t8[1], t8[2], t8[3]);
-            xs[(2 * u + 1) * NT + tid] = make_float4(t8[4], t8[5], t8[6], t8[7]);
-        }
-#else
         float xf[VPT][8];   // the row as floats, unpacked once for all destinations
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
             unpack8((FULL || vi < a.nvec) ? ld_nc_v4(xrow + (int64_t)vi * 8) : make_uint4(0, 0, 0, 0), xf[u]);
         }
-#endif
         __syncthreads();
         const int nvd = snv;
         float4 sc[VPT][2];
@@ -164,15 +146,9 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
             for (int u = 0; u < VPT; ++u) {
                 const float s8[8] = {sc[u][0].x, sc[u][0].y, sc[u][0].z, sc[u][0].w,
                                      sc[u][1].x, sc[u][1].y, sc[u][1].z, sc[u][1].w};
-#if EP_SCALED_X_SMEM
-                const float4 x0 = xs[(2 * u) * NT + tid], x1 = xs[(2 * u + 1) * NT + tid];
-                const float x8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#else
-                const float* x8 = xf[u];
-#endif
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    f[u][i] = again ? mul_rn_again(x8[i], s8[i]) : __fmul_rn(x8[i], s8[i]);
+                    f[u][i] = again ? mul_rn_again(xf[u][i], s8[i]) : __fmul_rn(xf[u][i], s8[i]);
             }
         };
         for (int j = 0; j < nvd; ++j) {
@@ -285,11 +261,7 @@ template <int Q>
 cudaError_t launch_scaled_q(const ep_handle* h, const DispatchArgs& a, cudaStream_t st) {
     constexpr int EV = EP_EXPERT_SCALED_VPT;
     const int ent = ((a.nvec + EV - 1) / EV + 31) / 32 * 32;
-#if EP_SCALED_X_SMEM
-    const size_t smem = sizeof(int) * (size_t)((a.E + 1 + 3) & ~3) + sizeof(float4) * 2 * EV * (size_t)ent;
-#else
     const size_t smem = sizeof(int) * (size_t)(a.E + 1);
-#endif
     // every thread's VPT vectors lie inside the row: no bounds checks
     const bool full = (int64_t)ent * EV == a.nvec;
     int occ = 0;
