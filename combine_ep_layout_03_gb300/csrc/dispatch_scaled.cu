@@ -38,20 +38,6 @@ __device__ __forceinline__ float mul_rn_again(float a, float b) {
     return r;
 }
 
-#ifndef EP_SCALED_L1_KEEP
-#define EP_SCALED_L1_KEEP 0
-#endif
-#ifndef EP_SCALED_CARVEOUT_L1
-#define EP_SCALED_CARVEOUT_L1 0
-#endif
-// read-only 16-byte load that asks L1 to keep the line (evict_last)
-__device__ __forceinline__ float4 ld_nc_keep(const float4* p) {
-    float4 v;
-    asm("ld.global.nc.L1::evict_last.v4.f32 {%0, %1, %2, %3}, [%4];"
-        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-    return v;
-}
-
 // Round-to-nearest-even of v to an integer by one float32 addition: for
 // |v| < 2^22, fl(v + 1.5 * 2^23) lies in [2^23, 2^24), where the spacing of
 // float32 is 1, so the addition's own rounding (to nearest, ties to even;
@@ -109,13 +95,8 @@ __global__ void __maxnreg__(EP_SCALED_MAXNREG) dispatch_expert_scaled_kernel(Dis
         for (int u = 0; u < VPT; ++u) {
             const int vi = u * NT + tid;
             if (FULL || vi < a.nvec) {
-#if EP_SCALED_L1_KEEP
-                sc[u][0] = ld_nc_keep(srow + 2 * vi);
-                sc[u][1] = ld_nc_keep(srow + 2 * vi + 1);
-#else
                 sc[u][0] = __ldg(srow + 2 * vi);
                 sc[u][1] = __ldg(srow + 2 * vi + 1);
-#endif
             } else {
                 sc[u][0] = sc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -283,12 +264,6 @@ cudaError_t launch_scaled_q(const ep_handle* h, const DispatchArgs& a, cudaStrea
     const size_t smem = sizeof(int) * (size_t)(a.E + 1);
     // every thread's VPT vectors lie inside the row: no bounds checks
     const bool full = (int64_t)ent * EV == a.nvec;
-#if EP_SCALED_CARVEOUT_L1
-    cudaFuncSetAttribute(dispatch_expert_scaled_kernel<Q, EV, true>,
-                         cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxL1);
-    cudaFuncSetAttribute(dispatch_expert_scaled_kernel<Q, EV, false>,
-                         cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxL1);
-#endif
     int occ = 0;
     cudaError_t err = full ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                                  &occ, dispatch_expert_scaled_kernel<Q, EV, true>, ent, smem)
