@@ -21,13 +21,6 @@
 
 namespace {
 
-// Layouts of at most this many count CTAs skip the scan launch (the assign
-// kernel sums the expert columns itself): B x E column reads per CTA.
-#ifndef EP_LAYOUT_FUSED_MAX_BLOCKS
-#define EP_LAYOUT_FUSED_MAX_BLOCKS 32
-#endif
-constexpr int kLayoutFusedMaxBlocks = EP_LAYOUT_FUSED_MAX_BLOCKS;
-
 constexpr unsigned kFull = 0xffffffffu;
 
 // Expert id of entry i; an entry masked out by xActiveMask reads as -1.
@@ -161,12 +154,6 @@ layout_scan_kernel(LayoutArgs a) {
     }
 }
 
-// FUSED (small layouts, few CTAs): the scan kernel's work is done here
-// instead, so the layout takes two launches: every CTA sums the expert
-// columns of the count kernel's histograms itself (the totals, and the part
-// of the CTAs before it), and CTA 0 writes cnt, src_prefix, recv_cnt and
-// num_tokens_per_rank.  The histograms are read, never rewritten.
-template <bool FUSED>
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_assign_kernel(LayoutArgs a) {
     extern __shared__ int smem[];
@@ -177,48 +164,12 @@ layout_assign_kernel(LayoutArgs a) {
     int* base = al + E;             // [E+1] first global row of each expert
     int* scratch = base + E + 1;    // [NW+1]
     int* wc = scratch + NW + 1;     // [NW][E] per-warp running rows
-    int* pb = wc + NW * E;          // FUSED: [E] entries of CTAs before this one
 
     const int tid = threadIdx.x;
-    if constexpr (FUSED) {
-        const int B = a.B, C = a.C, bb = blockIdx.x;
-        for (int e = tid; e < E; e += blockDim.x) {
-            const int* col = a.blk_hist + (int64_t)e * B;
-            int before = 0, all = 0;
-            for (int b2 = 0; b2 < B; ++b2) {
-                const int v = col[b2];
-                before += b2 < bb ? v : 0;
-                all += v;
-            }
-            pb[e] = before;
-            rc[e] = all;
-            if (bb == 0) {
-                a.recv_cnt[e] = all;
-                int run = 0;
-                for (int s2 = 0; s2 < a.R; ++s2) {
-                    int cs = 0;
-                    for (int c2 = 0; c2 < C; ++c2) cs += col[s2 * C + c2];
-                    a.src_prefix[(int64_t)s2 * E + e] = run;
-                    a.cnt[(int64_t)s2 * E + e] = cs;
-                    run += cs;
-                }
-            }
-        }
-        if (bb == 0) {
-            for (int g = tid; g < a.R * a.R; g += blockDim.x) {
-                const int s2 = g / a.R, j = g - s2 * a.R;
-                int acc = 0;
-                for (int c2 = 0; c2 < C; ++c2) acc += a.blk_rank[((int64_t)s2 * C + c2) * a.R + j];
-                a.ntpr[g] = acc;
-            }
-        }
-        for (int e = tid; e < E; e += blockDim.x) al[e] = ((rc[e] + a.alpha - 1) / a.alpha) * a.alpha;
-    } else {
-        for (int e = tid; e < E; e += blockDim.x) {
-            const int c = a.recv_cnt[e];
-            rc[e] = c;
-            al[e] = ((c + a.alpha - 1) / a.alpha) * a.alpha;
-        }
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int c = a.recv_cnt[e];
+        rc[e] = c;
+        al[e] = ((c + a.alpha - 1) / a.alpha) * a.alpha;
     }
     __syncthreads();
     block_exclusive_scan(al, base, E, scratch);
@@ -279,7 +230,7 @@ layout_assign_kernel(LayoutArgs a) {
     __syncthreads();
     // phase B: first row of each (warp, expert) = expert base + CTA prefix + earlier warps
     for (int e = tid; e < E; e += blockDim.x) {
-        int run = base[e] + (FUSED ? pb[e] : a.blk_hist[(int64_t)e * a.B + b]);
+        int run = base[e] + a.blk_hist[(int64_t)e * a.B + b];
         for (int w = 0; w < NW; ++w) {
             const int v = wc[w * E + e];
             wc[w * E + e] = run;
@@ -466,20 +417,15 @@ cudaError_t launch_layout(const ep_handle* h, const int64_t* topk, const uint8_t
     const size_t smem_count = sizeof(int) * (size_t)(h->E + h->R);
     layout_count_kernel<<<h->B, kLayoutThreads, smem_count, st>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    constexpr int NW = kLayoutThreads / 32;
-    const size_t smem_assign = sizeof(int) * (size_t)(3 * h->E + 1 + NW + 1 + NW * h->E);
-    if (h->B <= kLayoutFusedMaxBlocks) {
-        // few CTAs: each sums its expert prefixes itself, no scan launch
-        layout_assign_kernel<true><<<h->B, kLayoutThreads, smem_assign + sizeof(int) * (size_t)h->E, st>>>(a);
-        return cudaGetLastError();
-    }
     const int64_t pairs = (int64_t)h->R * h->R;
-    int64_t rank_ctas = (pairs + NW - 1) / NW;
+    int64_t rank_ctas = (pairs + (kLayoutThreads / 32) - 1) / (kLayoutThreads / 32);
     if (rank_ctas > 1024) rank_ctas = 1024;
-    const size_t smem_scan = sizeof(int) * (size_t)(2 * h->B + 1 + NW + 1);
+    const size_t smem_scan = sizeof(int) * (size_t)(2 * h->B + 1 + kLayoutThreads / 32 + 1);
     layout_scan_kernel<<<(unsigned)(h->E + rank_ctas), kLayoutThreads, smem_scan, st>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    layout_assign_kernel<false><<<h->B, kLayoutThreads, smem_assign, st>>>(a);
+    constexpr int NW = kLayoutThreads / 32;
+    const size_t smem_assign = sizeof(int) * (size_t)(3 * h->E + 1 + NW + 1 + NW * h->E);
+    layout_assign_kernel<<<h->B, kLayoutThreads, smem_assign, st>>>(a);
     return cudaGetLastError();
 }
 
