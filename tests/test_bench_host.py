@@ -4,8 +4,6 @@ the committed ncu summary (a row counts only for the source it was taken on)."""
 import os
 import sys
 
-import pytest
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import GpuPath, bf16_bits, compare_layout, to_dev_bf16
+from gpu_harness import GpuPath, compare_layout, to_dev_bf16
 from test_gpu_parity import check_combine, check_dispatch
 
 pytestmark = pytest.mark.gpu

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from combine_ep_layout_03_gb300 import ep, synth
-from gpu_harness import GpuPath, bf16_bits, compare_layout, oracle_combine_sampled, to_dev_bf16
+from gpu_harness import GpuPath, bf16_bits, compare_layout, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 

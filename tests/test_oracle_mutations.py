@@ -9,7 +9,6 @@ import contextlib
 import os
 import subprocess
 
-import numpy as np
 import pytest
 
 import oracle

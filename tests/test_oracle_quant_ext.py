@@ -9,8 +9,6 @@ rational arithmetic for the scale and the product with torch's float8 cast for
 the element code, exact rationals for static int8, scale invariances, and the
 brute-force layout for masks.
 """
-import math
-import os
 from fractions import Fraction
 
 import numpy as np
